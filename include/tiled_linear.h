@@ -1,0 +1,184 @@
+/*
+ * tiled_linear.h -- C ABI of a host-streamed, output-tiled linear operator for
+ * one GB300 GPU (sm_103a).
+ *
+ * The operator is Y = X.W with W [K, M] too large to keep on the device.  W is
+ * split along its output dimension into N tiles W_1..W_N of Mi = M/N columns;
+ * the forward pass computes Y_i = X.W_i one tile at a time and the column
+ * blocks Y_i together are Y, with no cross-tile term (pwwt.cn/news/5430303,
+ * "关键技术一: Memory-centric tiling", 核心思想; aicassindra
+ * tm_zero_infinity, "Memory-centric tiling: operators bigger than the
+ * device").  Each tile lives in pinned host memory and is copied into a ring
+ * of device slots up to d tiles ahead of the tile being computed, with the
+ * depth rule d >= t_fetch / t_layer (tm_zero_infinity, "Prefetch depth: how
+ * far ahead the pipeline must run").  A slot is reused as soon as its last
+ * reader finishes (the gathered weights are released after use:
+ * gpu_zero_sharding, "End-to-end flow").  Backward fetches every tile again,
+ * computes dW_i = X^T.dY_i and writes it back to pinned host memory on a
+ * second copy stream while later tiles compute (pwwt.cn/news/5430303,
+ * "关键技术三", 后向传播中的重叠), and accumulates dX += dY_i.W_i^T in fp32.
+ *
+ * Conventions for every function:
+ *  - All matrices are row-major, bf16 stored as 16-bit patterns unless stated.
+ *  - "_dev" pointers are device memory of the handle's device; "_host"
+ *    pointers are pinned host memory (cudaHostAlloc / cudaHostRegister or
+ *    tiled_linear_host_alloc).  The caller owns every buffer it passes.
+ *  - A `stream` argument is a cudaStream_t passed as void* (NULL = legacy
+ *    default stream).  Work is enqueued and the call returns; results are
+ *    valid once `stream` has completed.
+ *  - Errors are returned as tl_status; nothing is thrown across the ABI.  A
+ *    CUDA failure inside a call makes the handle sticky-failed: later calls
+ *    return TL_ERR_STATE and tiled_linear_last_error() keeps the message.
+ *  - A handle is not thread-safe: use one handle per thread.
+ *  - No function here allocates device memory; the caller supplies it.
+ */
+#ifndef TILED_LINEAR_H
+#define TILED_LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tl_handle tl_handle;
+
+typedef enum {
+    TL_OK = 0,
+    TL_ERR_INVALID = 1,     /* bad shape, depth, pointer or alignment        */
+    TL_ERR_NOT_PINNED = 2,  /* w_host / dw_host is not pinned host memory    */
+    TL_ERR_WORKSPACE = 3,   /* workspace too small or misaligned             */
+    TL_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed           */
+    TL_ERR_TIMEOUT = 5,     /* a kernel's bounded wait gave up (see below)   */
+    TL_ERR_STATE = 6        /* handle already failed, or NULL                */
+} tl_status;
+
+/* Host storage of W (read) and dW (written).
+ *  ROW_MAJOR : logical [K, M] row-major; tile i is a strided column block
+ *              (copied with pitched 2-D copies).
+ *  TILE_MAJOR: [N][K][Mi]; tile i is one contiguous K*Mi block (copied with
+ *              1-D copies, which keep the full host-link bandwidth). */
+typedef enum { TL_LAYOUT_ROW_MAJOR = 0, TL_LAYOUT_TILE_MAJOR = 1 } tl_layout;
+
+/* Per-call timings, from CUDA events the library records on the streams that
+ * run the work.  Times in milliseconds; *_gemm_ms are sums over the tiles of
+ * the kernel's own span on the compute stream; *_copy_ms are sums of the copy
+ * spans on the copy streams; *_total_ms spans the whole call on `stream`. */
+typedef struct {
+    int32_t n_tiles;
+    int32_t depth;            /* d used by the call                           */
+    int32_t fwd_valid, bwd_valid;
+    float fwd_total_ms, fwd_gemm_ms, fwd_h2d_ms;
+    float bwd_total_ms, bwd_dw_gemm_ms, bwd_dx_gemm_ms, bwd_h2d_ms, bwd_d2h_ms;
+    float fwd_wait_ms;        /* fwd_total - fwd_gemm: compute stream idle    */
+    float bwd_wait_ms;        /* bwd_total - both GEMM sums                   */
+    int64_t fwd_h2d_bytes, bwd_h2d_bytes, bwd_d2h_bytes;
+    int32_t fwd_launches, bwd_launches;   /* kernels launched by the call     */
+} tl_stats;
+
+/* Device workspace bytes needed for (K, M, N, d): (min(d,N-1)+1) weight slots
+ * and min(2,N) gradient staging slots of K*(M/N) bf16 each, plus a 4 KiB
+ * header.  d = -1 (automatic depth) sizes for d = min(N-1, 3).  Returns 0 if
+ * the arguments are invalid. */
+size_t tiled_linear_workspace_bytes(int64_t K, int64_t M, int32_t N, int32_t d);
+
+/* Create a handle on `device`.
+ *  K, M, N : W is [K, M] bf16, split into N tiles of Mi = M/N columns.
+ *            Requires K >= 8, K % 8 == 0, M % N == 0, Mi % 8 == 0 (16-byte
+ *            row pitches for the tensor-memory-access engine).
+ *  d       : tiles fetched ahead of the one being computed (ring of d+1
+ *            slots; d >= N-1 keeps every tile resident).  d = 0 serialises
+ *            copy and compute.  d = -1 picks d = ceil(t_fetch / t_layer) from
+ *            the first forward call's measured copy and kernel times, bounded
+ *            by the workspace.
+ *  w_host  : pinned host W (read by every call; must not change while a
+ *            call is in flight).  dw_host: pinned host dW (overwritten by
+ *            every backward call).  Both in tiled_linear_create's layout:
+ *            TL_LAYOUT_ROW_MAJOR.  May alias nothing else the call writes.
+ *  workspace_dev, workspace_bytes: device memory, 256-byte aligned, at least
+ *            tiled_linear_workspace_bytes(K, M, N, d); owned by the caller,
+ *            used until tiled_linear_destroy returns.
+ * Errors: TL_ERR_INVALID (shapes/pointers), TL_ERR_NOT_PINNED,
+ * TL_ERR_WORKSPACE, TL_ERR_CUDA.  On error *out is set to NULL. */
+tl_status tiled_linear_create(tl_handle **out, int64_t K, int64_t M, int32_t N, int32_t d,
+                              const void *w_host, void *dw_host,
+                              void *workspace_dev, size_t workspace_bytes, int device);
+
+/* As tiled_linear_create, with W and dW stored tile-major [N][K][Mi]. */
+tl_status tiled_linear_create_tilemajor(tl_handle **out, int64_t K, int64_t M, int32_t N,
+                                        int32_t d, const void *w_host, void *dw_host,
+                                        void *workspace_dev, size_t workspace_bytes,
+                                        int device);
+
+/* Forward: y_dev[T, M] (bf16, ld M) = x_dev[T, K] (bf16, ld K) . W, tile by
+ * tile, fp32 accumulation, round-to-nearest-even to bf16.  T >= 0 (T = 0 is
+ * a no-op).  Weight copies may begin before earlier work on `stream`
+ * finishes (they only read w_host).  Errors: TL_ERR_INVALID, TL_ERR_STATE,
+ * TL_ERR_CUDA, TL_ERR_TIMEOUT (a previous call's kernel timed out). */
+tl_status tiled_linear_forward(tl_handle *h, int64_t T, const void *x_dev, void *y_dev,
+                               void *stream);
+
+/* Backward, tiles in descending order i = N-1 .. 0:
+ *   dW_i = X^T . dY_i  (fp32 accumulation, bf16 RNE) -> dw_host tile i
+ *   dx_dev[T, K] (fp32, ld K) = sum_i dY_i . W_i^T   (overwritten: the first
+ *   tile stores, later tiles add, in this fixed order)
+ * dy_dev is [T, M] bf16 (ld M).  T = 0 writes dW = 0.  dW on the host is
+ * complete once `stream` has completed.  Errors as tiled_linear_forward. */
+tl_status tiled_linear_backward(tl_handle *h, int64_t T, const void *x_dev,
+                                const void *dy_dev, float *dx_dev, void *stream);
+
+/* Synchronise the handle's streams, release its streams and events and free
+ * the handle.  The caller's buffers are untouched.  Returns the handle's
+ * sticky status (TL_OK if it never failed).  NULL is accepted (TL_OK). */
+tl_status tiled_linear_destroy(tl_handle *h);
+
+/* Message of the last failure on h ("" if none); a static message for NULL. */
+const char *tiled_linear_last_error(const tl_handle *h);
+
+/* Wait for the handle's last forward and backward calls to finish, check the
+ * kernels' timeout word, and fill *out (a tl_stats).  Returns TL_ERR_TIMEOUT
+ * if a kernel gave up waiting. */
+tl_status tiled_linear_get_stats(tl_handle *h, void *tl_stats_out);
+
+/* --- resident GEMMs: the three kernels on device-resident operands --------
+ * The same kernels the engine launches per tile, for callers that already
+ * hold a tile on the device.  fp32 accumulation in tensor memory; err_dev is
+ * a device int32 the kernel sets non-zero if a bounded wait gives up (it is
+ * only ever OR-ed into, never cleared).  Requirements: every leading
+ * dimension and column offset a multiple of 8 elements, pointers 16-byte
+ * aligned, all sizes >= 1.  Errors: TL_ERR_INVALID, TL_ERR_CUDA. */
+
+/* y[T, n] (bf16, ld ldy) = x[T, K] (bf16, ld ldx) . w[K, n] (bf16, ld ldw). */
+tl_status tiled_linear_gemm_forward(int64_t T, int64_t K, int64_t n,
+                                    const void *x_dev, int64_t ldx,
+                                    const void *w_dev, int64_t ldw,
+                                    void *y_dev, int64_t ldy, int32_t *err_dev, void *stream);
+
+/* dw[K, n] (bf16, ld lddw) = x[T, K]^T (bf16, ld ldx) . dy[T, n] (bf16, ld lddy). */
+tl_status tiled_linear_gemm_dw(int64_t T, int64_t K, int64_t n,
+                               const void *x_dev, int64_t ldx,
+                               const void *dy_dev, int64_t lddy,
+                               void *dw_dev, int64_t lddw, int32_t *err_dev, void *stream);
+
+/* dx[T, K] (fp32, ld lddx) (+)= dy[T, n] (bf16, ld lddy) . w[K, n]^T (bf16,
+ * ld ldw); accumulate = 0 overwrites dx, 1 adds to it. */
+tl_status tiled_linear_gemm_dx(int64_t T, int64_t K, int64_t n,
+                               const void *dy_dev, int64_t lddy,
+                               const void *w_dev, int64_t ldw,
+                               float *dx_dev, int64_t lddx, int32_t accumulate,
+                               int32_t *err_dev, void *stream);
+
+/* --- pinned host memory helpers ------------------------------------------ */
+/* Page-locked host allocation (cudaHostAlloc, portable); *out = NULL on
+ * failure.  Free with tiled_linear_host_free. */
+tl_status tiled_linear_host_alloc(size_t bytes, void **out);
+tl_status tiled_linear_host_free(void *p);
+
+/* Library version string. */
+const char *tiled_linear_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TILED_LINEAR_H */

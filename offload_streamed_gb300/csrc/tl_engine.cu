@@ -1,0 +1,714 @@
+// tl_engine.cu -- the prefetch / eviction engine behind the C ABI.
+//
+// Resources per handle: two copy streams (host->device, device->host), a ring
+// of (d+1) device slots for weight tiles, min(2, N) device staging slots for
+// gradient tiles, and events that order them:
+//   ready[s]   copy of a tile into weight slot s has landed      (h2d -> compute)
+//   free[s]    last reader of weight slot s has finished         (compute -> h2d)
+//   dwdone[g]  gradient tile in staging slot g is complete       (compute -> d2h)
+//   drained[g] staging slot g has been copied back to the host   (d2h -> compute)
+// The copy of tile f into slot f % (d+1) waits for free[] of the fetch d+1
+// earlier, so the h2d stream runs up to d tiles ahead of the compute stream
+// (aicassindra tm_zero_infinity, "Prefetch depth: how far ahead the pipeline
+// must run"; pwwt.cn/news/5430303, "关键技术三", 动态预取器).  A slot whose
+// reader has finished is refilled: that is the release of the gathered
+// weights (gpu_zero_sharding, "End-to-end flow").  Backward runs the tiles in
+// descending order (the backward pass walks the operators in reverse: same
+// section), fetches every tile again (it was freed after forward), runs the
+// weight-gradient GEMM first (it does not read W_i, so it overlaps the
+// tile's fetch), hands the gradient tile to the d2h stream, and then
+// accumulates dX with the W_i tile (pwwt.cn/news/5430303, "关键技术三",
+// 后向传播中的重叠: gradients go back to slow memory while later operators
+// compute).
+#include "tiled_linear.h"
+#include "tl_gemm.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+namespace {
+
+constexpr size_t kHeaderBytes = 4096;
+constexpr size_t kAlign = 256;
+constexpr int kMaxStage = 2;
+constexpr int kAutoMaxDepth = 3;
+
+thread_local std::string g_create_error;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Shape {
+    int64_t K = 0, M = 0, Mi = 0;
+    int32_t N = 0;
+};
+
+// Shape rules shared by workspace sizing and create.  Empty string = valid.
+std::string check_shape(int64_t K, int64_t M, int32_t N, int32_t d) {
+    if (K < 8 || K % 8) return "K must be a positive multiple of 8";
+    if (M < 1 || N < 1) return "M and N must be >= 1";
+    if (M % N) return "M must be divisible by N";
+    if ((M / N) % 8) return "M/N (tile width) must be a multiple of 8";
+    if (d < -1) return "d must be >= -1";
+    if (K > (int64_t(1) << 31) || M > (int64_t(1) << 34)) return "K or M too large";
+    return {};
+}
+
+int32_t slots_for(int32_t N, int32_t d) {
+    const int32_t dd = d < 0 ? std::min(N - 1, kAutoMaxDepth) : std::min(d, N - 1);
+    return dd + 1;
+}
+
+size_t tile_bytes(int64_t K, int64_t Mi) { return size_t(K) * size_t(Mi) * 2; }
+
+struct CallTiming {
+    bool valid = false;
+    cudaEvent_t start = nullptr, end = nullptr;
+    // per tile: [0] kernel-1 start, [1] kernel-1 end, [2] kernel-2 start,
+    // [3] kernel-2 end, [4] h2d start, [5] h2d end, [6] d2h start, [7] d2h end
+    std::vector<cudaEvent_t> ev[8];
+    int32_t depth = 0;
+    int32_t launches = 0;
+    int64_t h2d_bytes = 0, d2h_bytes = 0;
+};
+
+}  // namespace
+
+struct tl_handle {
+    int device = 0;
+    Shape s;
+    tl_layout layout = TL_LAYOUT_ROW_MAJOR;
+    int32_t d_req = 0, d = 0, slot_cap = 0, nstage = 0;
+    bool auto_pending = false;
+    const uint8_t* w_host = nullptr;
+    uint8_t* dw_host = nullptr;
+    uint8_t* ws = nullptr;
+    size_t ws_bytes = 0;
+    int32_t* err_dev = nullptr;
+    int32_t* err_mirror = nullptr;  // pinned host copy of *err_dev, refreshed per call
+    std::vector<uint8_t*> slot, stage;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    std::vector<cudaEvent_t> ev_ready, ev_free, ev_dwdone, ev_drained;
+    uint64_t fetch_seq = 0, stage_seq = 0;
+    int num_sms = 0;
+    CallTiming fwd, bwd;
+    tl_status sticky = TL_OK;
+    std::string msg;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) err = cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+tl_status fail(tl_handle* h, tl_status st, const std::string& what) {
+    if (h) {
+        h->msg = what;
+        if (st == TL_ERR_CUDA || st == TL_ERR_TIMEOUT) h->sticky = st;
+    }
+    return st;
+}
+
+#define TL_TRY(h, call)                                                                   \
+    do {                                                                                  \
+        cudaError_t e_ = (call);                                                          \
+        if (e_ != cudaSuccess)                                                            \
+            return fail((h), TL_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+    } while (0)
+
+bool is_pinned_host(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+bool is_device_mem(const void* p, int device) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == device;
+}
+
+tl_status create_events(tl_handle* h, CallTiming& t, int n) {
+    TL_TRY(h, cudaEventCreate(&t.start));
+    TL_TRY(h, cudaEventCreate(&t.end));
+    for (auto& v : t.ev) {
+        v.assign(size_t(n), nullptr);
+        for (auto& e : v) TL_TRY(h, cudaEventCreate(&e));
+    }
+    return TL_OK;
+}
+
+void destroy_events(CallTiming& t) {
+    if (t.start) cudaEventDestroy(t.start);
+    if (t.end) cudaEventDestroy(t.end);
+    for (auto& v : t.ev)
+        for (auto e : v)
+            if (e) cudaEventDestroy(e);
+}
+
+// Read the pinned mirror of the kernels' error word (written at the end of
+// every call); a non-zero word makes the handle sticky-failed.
+tl_status poll_error(tl_handle* h) {
+    if (h->err_mirror && *reinterpret_cast<volatile int32_t*>(h->err_mirror) != 0)
+        return fail(h, TL_ERR_TIMEOUT,
+                    "a kernel's bounded wait timed out (error bits " +
+                        std::to_string(*h->err_mirror) + ")");
+    return TL_OK;
+}
+
+tl_status check_usable(tl_handle* h) {
+    if (!h) return TL_ERR_STATE;
+    if (h->sticky != TL_OK) return TL_ERR_STATE;
+    return poll_error(h);
+}
+
+const uint8_t* w_tile_src(const tl_handle* h, int i) {
+    const Shape& s = h->s;
+    if (h->layout == TL_LAYOUT_TILE_MAJOR) return h->w_host + size_t(i) * tile_bytes(s.K, s.Mi);
+    return h->w_host + size_t(i) * size_t(s.Mi) * 2;
+}
+
+uint8_t* dw_tile_dst(const tl_handle* h, int i) {
+    const Shape& s = h->s;
+    if (h->layout == TL_LAYOUT_TILE_MAJOR) return h->dw_host + size_t(i) * tile_bytes(s.K, s.Mi);
+    return h->dw_host + size_t(i) * size_t(s.Mi) * 2;
+}
+
+cudaError_t copy_w_tile(const tl_handle* h, int i, void* dst, cudaStream_t st) {
+    const Shape& s = h->s;
+    if (h->layout == TL_LAYOUT_TILE_MAJOR)
+        return cudaMemcpyAsync(dst, w_tile_src(h, i), tile_bytes(s.K, s.Mi), cudaMemcpyHostToDevice, st);
+    return cudaMemcpy2DAsync(dst, size_t(s.Mi) * 2, w_tile_src(h, i), size_t(s.M) * 2,
+                             size_t(s.Mi) * 2, size_t(s.K), cudaMemcpyHostToDevice, st);
+}
+
+cudaError_t copy_dw_tile(const tl_handle* h, int i, const void* src, cudaStream_t st) {
+    const Shape& s = h->s;
+    if (h->layout == TL_LAYOUT_TILE_MAJOR)
+        return cudaMemcpyAsync(dw_tile_dst(h, i), src, tile_bytes(s.K, s.Mi), cudaMemcpyDeviceToHost, st);
+    return cudaMemcpy2DAsync(dw_tile_dst(h, i), size_t(s.M) * 2, src, size_t(s.Mi) * 2,
+                             size_t(s.Mi) * 2, size_t(s.K), cudaMemcpyDeviceToHost, st);
+}
+
+float span_ms(cudaEvent_t a, cudaEvent_t b) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) {
+        cudaGetLastError();
+        return 0.f;
+    }
+    return ms;
+}
+
+// Automatic depth: after the first forward call, d = ceil(t_fetch / t_layer)
+// from that call's measured copy and kernel spans (tm_zero_infinity,
+// "Prefetch depth"), bounded by the slots the workspace holds.
+tl_status finish_auto_depth(tl_handle* h) {
+    if (!h->auto_pending || !h->fwd.valid) return TL_OK;
+    TL_TRY(h, cudaEventSynchronize(h->fwd.end));
+    const int n = h->s.N;
+    double fetch = 0, layer = 0;
+    for (int i = 0; i < n; ++i) {
+        fetch += span_ms(h->fwd.ev[4][i], h->fwd.ev[5][i]);
+        layer += span_ms(h->fwd.ev[0][i], h->fwd.ev[1][i]);
+    }
+    int32_t dnew = 1;
+    if (layer > 0) dnew = int32_t(std::ceil(fetch / layer));
+    dnew = std::max<int32_t>(1, std::min<int32_t>(dnew, h->slot_cap - 1));
+    if (h->slot_cap - 1 < 1) dnew = 0;
+    if (dnew != h->d) {
+        for (int s = 0; s < h->slot_cap; ++s) TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[s], 0));
+        h->d = dnew;
+        h->fetch_seq = 0;
+    }
+    h->auto_pending = false;
+    return TL_OK;
+}
+
+tl_status launch(tl_handle* h, const tl::GemmDesc& g, cudaStream_t st) {
+    std::string why;
+    cudaError_t e = tl::gemm_launch(g, h->num_sms, st, &why);
+    if (e != cudaSuccess) return fail(h, TL_ERR_CUDA, "GEMM launch: " + why);
+    return TL_OK;
+}
+
+tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t d,
+                      const void* w_host, void* dw_host, void* ws, size_t ws_bytes, int device,
+                      tl_layout layout) {
+    if (!out) {
+        g_create_error = "out is NULL";
+        return TL_ERR_INVALID;
+    }
+    *out = nullptr;
+    std::string bad = check_shape(K, M, N, d);
+    if (bad.empty() && (!w_host || !dw_host || !ws)) bad = "null pointer argument";
+    if (bad.empty() && device < 0) bad = "device must be >= 0";
+    if (!bad.empty()) {
+        g_create_error = bad;
+        return TL_ERR_INVALID;
+    }
+    const size_t need = tiled_linear_workspace_bytes(K, M, N, d);
+    if (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % kAlign)) {
+        g_create_error = "workspace too small or not 256-byte aligned (need " + std::to_string(need) +
+                         " bytes)";
+        return TL_ERR_WORKSPACE;
+    }
+
+    tl_handle* h = new (std::nothrow) tl_handle();
+    if (!h) {
+        g_create_error = "out of host memory";
+        return TL_ERR_INVALID;
+    }
+    auto bail = [&](tl_status st) {
+        g_create_error = h->msg;
+        tiled_linear_destroy(h);
+        return st;
+    };
+    h->device = device;
+    h->s.K = K;
+    h->s.M = M;
+    h->s.N = N;
+    h->s.Mi = M / N;
+    h->layout = layout;
+    h->d_req = d;
+    h->w_host = static_cast<const uint8_t*>(w_host);
+    h->dw_host = static_cast<uint8_t*>(dw_host);
+    h->ws = static_cast<uint8_t*>(ws);
+    h->ws_bytes = ws_bytes;
+
+    DeviceGuard guard(device);
+    if (guard.err != cudaSuccess) {
+        h->msg = std::string("cudaSetDevice: ") + cudaGetErrorString(guard.err);
+        return bail(TL_ERR_CUDA);
+    }
+    if (!is_pinned_host(w_host) || !is_pinned_host(dw_host)) {
+        h->msg = "w_host and dw_host must be pinned host memory";
+        return bail(TL_ERR_NOT_PINNED);
+    }
+    if (!is_device_mem(ws, device)) {
+        h->msg = "workspace is not device memory of the handle's device";
+        return bail(TL_ERR_WORKSPACE);
+    }
+
+    // Carve the workspace: header (error word), weight slots, staging slots.
+    const size_t tb = align_up(tile_bytes(K, M / N), kAlign);
+    const int32_t min_slots = slots_for(N, d);
+    const int32_t fit = int32_t(std::min<size_t>(size_t(N), (ws_bytes - kHeaderBytes) / tb - size_t(std::min(N, kMaxStage))));
+    h->nstage = std::min(N, kMaxStage);
+    h->slot_cap = d < 0 ? std::max(min_slots, std::min(fit, kAutoMaxDepth + 1)) : min_slots;
+    h->slot_cap = std::min<int32_t>(h->slot_cap, N);
+    h->d = h->slot_cap - 1;
+    h->auto_pending = (d < 0);
+    h->err_dev = reinterpret_cast<int32_t*>(h->ws);
+    uint8_t* p = h->ws + kHeaderBytes;
+    for (int s = 0; s < h->slot_cap; ++s, p += tb) h->slot.push_back(p);
+    for (int g = 0; g < h->nstage; ++g, p += tb) h->stage.push_back(p);
+
+    if (cudaMemset(h->err_dev, 0, sizeof(int32_t)) != cudaSuccess ||
+        cudaHostAlloc(reinterpret_cast<void**>(&h->err_mirror), sizeof(int32_t), cudaHostAllocPortable) !=
+            cudaSuccess) {
+        h->msg = std::string("error-word setup: ") + cudaGetErrorString(cudaGetLastError());
+        return bail(TL_ERR_CUDA);
+    }
+    *h->err_mirror = 0;
+    if (cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking) != cudaSuccess) {
+        h->msg = std::string("stream creation: ") + cudaGetErrorString(cudaGetLastError());
+        return bail(TL_ERR_CUDA);
+    }
+    auto mk = [&](std::vector<cudaEvent_t>& v, int n) {
+        v.assign(size_t(n), nullptr);
+        for (auto& e : v)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+        return true;
+    };
+    if (!mk(h->ev_ready, h->slot_cap) || !mk(h->ev_free, h->slot_cap) || !mk(h->ev_dwdone, h->nstage) ||
+        !mk(h->ev_drained, h->nstage)) {
+        h->msg = std::string("event creation: ") + cudaGetErrorString(cudaGetLastError());
+        return bail(TL_ERR_CUDA);
+    }
+    if (create_events(h, h->fwd, N) != TL_OK || create_events(h, h->bwd, N) != TL_OK)
+        return bail(TL_ERR_CUDA);
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        h->msg = "cudaDeviceGetAttribute(multiProcessorCount) failed";
+        return bail(TL_ERR_CUDA);
+    }
+    *out = h;
+    return TL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tiled_linear_workspace_bytes(int64_t K, int64_t M, int32_t N, int32_t d) {
+    if (!check_shape(K, M, N, d).empty()) return 0;
+    const size_t tb = align_up(tile_bytes(K, M / N), kAlign);
+    return kHeaderBytes + size_t(slots_for(N, d) + std::min(N, kMaxStage)) * tb;
+}
+
+tl_status tiled_linear_create(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t d,
+                              const void* w_host, void* dw_host, void* workspace_dev,
+                              size_t workspace_bytes, int device) {
+    return create_impl(out, K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes, device,
+                       TL_LAYOUT_ROW_MAJOR);
+}
+
+tl_status tiled_linear_create_tilemajor(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t d,
+                                        const void* w_host, void* dw_host, void* workspace_dev,
+                                        size_t workspace_bytes, int device) {
+    return create_impl(out, K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes, device,
+                       TL_LAYOUT_TILE_MAJOR);
+}
+
+tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void* y_dev, void* stream) {
+    tl_status st = check_usable(h);
+    if (st != TL_OK) return st;
+    if (T < 0 || T > (int64_t(1) << 30)) return fail(h, TL_ERR_INVALID, "T out of range");
+    if (T == 0) return TL_OK;
+    if (!x_dev || !y_dev) return fail(h, TL_ERR_INVALID, "null x or y");
+    if ((reinterpret_cast<uintptr_t>(x_dev) | reinterpret_cast<uintptr_t>(y_dev)) & 15u)
+        return fail(h, TL_ERR_INVALID, "x and y must be 16-byte aligned");
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return fail(h, TL_ERR_CUDA, "cudaSetDevice failed");
+    if ((st = finish_auto_depth(h)) != TL_OK) return st;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const Shape& s = h->s;
+    CallTiming& t = h->fwd;
+    const int nslots = h->d + 1;
+    TL_TRY(h, cudaEventRecord(t.start, cs));
+    for (int i = 0; i < s.N; ++i) {
+        const int sl = int(h->fetch_seq++ % uint64_t(nslots));
+        TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
+        TL_TRY(h, cudaEventRecord(t.ev[4][i], h->h2d));
+        TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
+        TL_TRY(h, cudaEventRecord(t.ev[5][i], h->h2d));
+        TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
+
+        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
+        TL_TRY(h, cudaEventRecord(t.ev[0][i], cs));
+        tl::GemmDesc g;
+        g.m_dim = T;
+        g.n_dim = s.Mi;
+        g.k_dim = s.K;
+        g.a = x_dev;
+        g.lda = s.K;
+        g.a_mn_major = false;
+        g.b = h->slot[sl];
+        g.ldb = s.Mi;
+        g.b_mn_major = true;
+        g.d = static_cast<uint8_t*>(y_dev) + size_t(i) * size_t(s.Mi) * 2;
+        g.ldd = s.M;
+        g.out = tl::OutKind::BF16;
+        g.err = h->err_dev;
+        if ((st = launch(h, g, cs)) != TL_OK) return st;
+        TL_TRY(h, cudaEventRecord(t.ev[1][i], cs));
+        TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
+    }
+    TL_TRY(h, cudaEventRecord(t.end, cs));
+    TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    t.valid = true;
+    t.depth = h->d;
+    t.launches = s.N;
+    t.h2d_bytes = int64_t(s.N) * int64_t(tile_bytes(s.K, s.Mi));
+    t.d2h_bytes = 0;
+    return TL_OK;
+}
+
+tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, const void* dy_dev,
+                                float* dx_dev, void* stream) {
+    tl_status st = check_usable(h);
+    if (st != TL_OK) return st;
+    if (T < 0 || T > (int64_t(1) << 30)) return fail(h, TL_ERR_INVALID, "T out of range");
+    if (T > 0 && (!x_dev || !dy_dev || !dx_dev)) return fail(h, TL_ERR_INVALID, "null x, dy or dx");
+    if ((reinterpret_cast<uintptr_t>(x_dev) | reinterpret_cast<uintptr_t>(dy_dev) |
+         reinterpret_cast<uintptr_t>(dx_dev)) & 15u)
+        return fail(h, TL_ERR_INVALID, "x, dy and dx must be 16-byte aligned");
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return fail(h, TL_ERR_CUDA, "cudaSetDevice failed");
+    if ((st = finish_auto_depth(h)) != TL_OK) return st;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const Shape& s = h->s;
+    const size_t tb = tile_bytes(s.K, s.Mi);
+    CallTiming& t = h->bwd;
+
+    if (T == 0) {  // dW = X^T dY over an empty sum: zero
+        TL_TRY(h, cudaEventRecord(t.start, cs));
+        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[0], 0));
+        TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tb, cs));
+        for (int i = 0; i < s.N; ++i) TL_TRY(h, copy_dw_tile(h, i, h->stage[0], cs));
+        TL_TRY(h, cudaEventRecord(h->ev_drained[0], cs));
+        TL_TRY(h, cudaEventRecord(t.end, cs));
+        t.valid = false;
+        return TL_OK;
+    }
+
+    const int nslots = h->d + 1;
+    TL_TRY(h, cudaEventRecord(t.start, cs));
+    for (int j = 0; j < s.N; ++j) {
+        const int i = s.N - 1 - j;
+        const int sl = int(h->fetch_seq++ % uint64_t(nslots));
+        const int gs = int(h->stage_seq++ % uint64_t(h->nstage));
+        // refetch W_i
+        TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
+        TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
+        TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
+        TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
+        TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
+
+        // dW_i = X^T dY_i into staging slot gs (does not need W_i)
+        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gs], 0));
+        TL_TRY(h, cudaEventRecord(t.ev[0][j], cs));
+        tl::GemmDesc gw;
+        gw.m_dim = s.K;
+        gw.n_dim = s.Mi;
+        gw.k_dim = T;
+        gw.a = x_dev;
+        gw.lda = s.K;
+        gw.a_mn_major = true;
+        gw.b = static_cast<const uint8_t*>(dy_dev) + size_t(i) * size_t(s.Mi) * 2;
+        gw.ldb = s.M;
+        gw.b_mn_major = true;
+        gw.d = h->stage[gs];
+        gw.ldd = s.Mi;
+        gw.out = tl::OutKind::BF16;
+        gw.err = h->err_dev;
+        if ((st = launch(h, gw, cs)) != TL_OK) return st;
+        TL_TRY(h, cudaEventRecord(t.ev[1][j], cs));
+        TL_TRY(h, cudaEventRecord(h->ev_dwdone[gs], cs));
+
+        // write dW_i back on the d2h stream
+        TL_TRY(h, cudaStreamWaitEvent(h->d2h, h->ev_dwdone[gs], 0));
+        TL_TRY(h, cudaEventRecord(t.ev[6][j], h->d2h));
+        TL_TRY(h, copy_dw_tile(h, i, h->stage[gs], h->d2h));
+        TL_TRY(h, cudaEventRecord(t.ev[7][j], h->d2h));
+        TL_TRY(h, cudaEventRecord(h->ev_drained[gs], h->d2h));
+
+        // dX (+)= dY_i W_i^T, fp32; the first tile of the pass stores
+        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
+        TL_TRY(h, cudaEventRecord(t.ev[2][j], cs));
+        tl::GemmDesc gx;
+        gx.m_dim = T;
+        gx.n_dim = s.K;
+        gx.k_dim = s.Mi;
+        gx.a = static_cast<const uint8_t*>(dy_dev) + size_t(i) * size_t(s.Mi) * 2;
+        gx.lda = s.M;
+        gx.a_mn_major = false;
+        gx.b = h->slot[sl];
+        gx.ldb = s.Mi;
+        gx.b_mn_major = false;
+        gx.d = dx_dev;
+        gx.ldd = s.K;
+        gx.out = tl::OutKind::F32;
+        gx.accumulate = (j > 0);
+        gx.err = h->err_dev;
+        if ((st = launch(h, gx, cs)) != TL_OK) return st;
+        TL_TRY(h, cudaEventRecord(t.ev[3][j], cs));
+        TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
+    }
+    // dW on the host is complete when `stream` is.
+    for (int g = 0; g < h->nstage; ++g) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[g], 0));
+    TL_TRY(h, cudaEventRecord(t.end, cs));
+    TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    t.valid = true;
+    t.depth = h->d;
+    t.launches = 2 * s.N;
+    t.h2d_bytes = int64_t(s.N) * int64_t(tb);
+    t.d2h_bytes = int64_t(s.N) * int64_t(tb);
+    return TL_OK;
+}
+
+tl_status tiled_linear_destroy(tl_handle* h) {
+    if (!h) return TL_OK;
+    tl_status st = h->sticky;
+    {
+        DeviceGuard guard(h->device);
+        if (h->h2d) cudaStreamSynchronize(h->h2d);
+        if (h->d2h) cudaStreamSynchronize(h->d2h);
+        for (auto* v : {&h->ev_ready, &h->ev_free, &h->ev_dwdone, &h->ev_drained})
+            for (auto e : *v) {
+                if (e) {
+                    cudaEventSynchronize(e);
+                    cudaEventDestroy(e);
+                }
+            }
+        if (h->fwd.end) cudaEventSynchronize(h->fwd.end);
+        if (h->bwd.end) cudaEventSynchronize(h->bwd.end);
+        destroy_events(h->fwd);
+        destroy_events(h->bwd);
+        if (h->h2d) cudaStreamDestroy(h->h2d);
+        if (h->d2h) cudaStreamDestroy(h->d2h);
+        if (h->err_mirror) cudaFreeHost(h->err_mirror);
+        cudaGetLastError();
+    }
+    delete h;
+    return st;
+}
+
+const char* tiled_linear_last_error(const tl_handle* h) {
+    if (!h) return g_create_error.c_str();
+    return h->msg.c_str();
+}
+
+tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
+    if (!h || !out_v) return TL_ERR_INVALID;
+    tl_stats* out = static_cast<tl_stats*>(out_v);
+    std::memset(out, 0, sizeof(*out));
+    DeviceGuard guard(h->device);
+    out->n_tiles = h->s.N;
+    out->depth = h->d;
+    const int n = h->s.N;
+    if (h->fwd.valid) {
+        TL_TRY(h, cudaEventSynchronize(h->fwd.end));
+        CallTiming& t = h->fwd;
+        out->fwd_valid = 1;
+        out->fwd_total_ms = span_ms(t.start, t.end);
+        for (int i = 0; i < n; ++i) {
+            out->fwd_gemm_ms += span_ms(t.ev[0][i], t.ev[1][i]);
+            out->fwd_h2d_ms += span_ms(t.ev[4][i], t.ev[5][i]);
+        }
+        out->fwd_wait_ms = out->fwd_total_ms - out->fwd_gemm_ms;
+        out->fwd_h2d_bytes = t.h2d_bytes;
+        out->fwd_launches = t.launches;
+        out->depth = t.depth;
+    }
+    if (h->bwd.valid) {
+        TL_TRY(h, cudaEventSynchronize(h->bwd.end));
+        CallTiming& t = h->bwd;
+        out->bwd_valid = 1;
+        out->bwd_total_ms = span_ms(t.start, t.end);
+        for (int j = 0; j < n; ++j) {
+            out->bwd_dw_gemm_ms += span_ms(t.ev[0][j], t.ev[1][j]);
+            out->bwd_dx_gemm_ms += span_ms(t.ev[2][j], t.ev[3][j]);
+            out->bwd_h2d_ms += span_ms(t.ev[4][j], t.ev[5][j]);
+            out->bwd_d2h_ms += span_ms(t.ev[6][j], t.ev[7][j]);
+        }
+        out->bwd_wait_ms = out->bwd_total_ms - out->bwd_dw_gemm_ms - out->bwd_dx_gemm_ms;
+        out->bwd_h2d_bytes = t.h2d_bytes;
+        out->bwd_d2h_bytes = t.d2h_bytes;
+        out->bwd_launches = t.launches;
+    }
+    int32_t word = 0;
+    TL_TRY(h, cudaMemcpy(&word, h->err_dev, sizeof(word), cudaMemcpyDeviceToHost));
+    if (word != 0)
+        return fail(h, TL_ERR_TIMEOUT,
+                    "a kernel's bounded wait timed out (error bits " + std::to_string(word) + ")");
+    return h->sticky;
+}
+
+// ---- resident GEMMs --------------------------------------------------------
+static tl_status raw_launch(const tl::GemmDesc& g, void* stream) {
+    std::string bad = tl::gemm_check(g);
+    if (!bad.empty()) return TL_ERR_INVALID;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TL_ERR_CUDA;
+    std::string why;
+    return tl::gemm_launch(g, sms, static_cast<cudaStream_t>(stream), &why) == cudaSuccess ? TL_OK
+                                                                                           : TL_ERR_CUDA;
+}
+
+tl_status tiled_linear_gemm_forward(int64_t T, int64_t K, int64_t n, const void* x_dev, int64_t ldx,
+                                    const void* w_dev, int64_t ldw, void* y_dev, int64_t ldy,
+                                    int32_t* err_dev, void* stream) {
+    tl::GemmDesc g;
+    g.m_dim = T;
+    g.n_dim = n;
+    g.k_dim = K;
+    g.a = x_dev;
+    g.lda = ldx;
+    g.a_mn_major = false;
+    g.b = w_dev;
+    g.ldb = ldw;
+    g.b_mn_major = true;
+    g.d = y_dev;
+    g.ldd = ldy;
+    g.out = tl::OutKind::BF16;
+    g.err = err_dev;
+    return raw_launch(g, stream);
+}
+
+tl_status tiled_linear_gemm_dw(int64_t T, int64_t K, int64_t n, const void* x_dev, int64_t ldx,
+                               const void* dy_dev, int64_t lddy, void* dw_dev, int64_t lddw,
+                               int32_t* err_dev, void* stream) {
+    tl::GemmDesc g;
+    g.m_dim = K;
+    g.n_dim = n;
+    g.k_dim = T;
+    g.a = x_dev;
+    g.lda = ldx;
+    g.a_mn_major = true;
+    g.b = dy_dev;
+    g.ldb = lddy;
+    g.b_mn_major = true;
+    g.d = dw_dev;
+    g.ldd = lddw;
+    g.out = tl::OutKind::BF16;
+    g.err = err_dev;
+    return raw_launch(g, stream);
+}
+
+tl_status tiled_linear_gemm_dx(int64_t T, int64_t K, int64_t n, const void* dy_dev, int64_t lddy,
+                               const void* w_dev, int64_t ldw, float* dx_dev, int64_t lddx,
+                               int32_t accumulate, int32_t* err_dev, void* stream) {
+    tl::GemmDesc g;
+    g.m_dim = T;
+    g.n_dim = K;
+    g.k_dim = n;
+    g.a = dy_dev;
+    g.lda = lddy;
+    g.a_mn_major = false;
+    g.b = w_dev;
+    g.ldb = ldw;
+    g.b_mn_major = false;
+    g.d = dx_dev;
+    g.ldd = lddx;
+    g.out = tl::OutKind::F32;
+    g.accumulate = accumulate != 0;
+    g.err = err_dev;
+    return raw_launch(g, stream);
+}
+
+tl_status tiled_linear_host_alloc(size_t bytes, void** out) {
+    if (!out) return TL_ERR_INVALID;
+    *out = nullptr;
+    if (bytes == 0) return TL_ERR_INVALID;
+    if (cudaHostAlloc(out, bytes, cudaHostAllocPortable) != cudaSuccess) {
+        cudaGetLastError();
+        *out = nullptr;
+        return TL_ERR_CUDA;
+    }
+    return TL_OK;
+}
+
+tl_status tiled_linear_host_free(void* p) {
+    if (!p) return TL_OK;
+    return cudaFreeHost(p) == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+}
+
+const char* tiled_linear_version(void) { return "tiled_linear 0.1 (sm_103a)"; }
+
+}  // extern "C"

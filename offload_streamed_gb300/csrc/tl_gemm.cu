@@ -1,0 +1,441 @@
+// tl_gemm.cu -- persistent, warp-specialised bf16 GEMM for sm_103a.
+//
+// One CTA per SM walks output tiles of 128 x 256 in a grouped raster order.
+//   warp 0      : TMA producer -- one thread loads the A and B slices of each
+//                 64-deep K-block into a 4-stage shared-memory ring.
+//   warp 1      : MMA issuer -- one thread issues tcgen05.mma (M=128, N=256,
+//                 K=16, bf16 x bf16 -> fp32) into one of two TMEM
+//                 accumulators, and frees a ring stage with tcgen05.commit.
+//   warp 2      : allocates / frees the 512 TMEM columns.
+//   warps 4..7  : epilogue -- tcgen05.ld of the finished accumulator (each
+//                 warp owns 32 TMEM lanes = 32 output rows), rounding to bf16
+//                 or storing / adding fp32, while the MMA warp already fills
+//                 the other accumulator.
+// There is no split of the reduction dimension: every output element is
+// reduced by one CTA in ascending K-block order, so a given element's value
+// does not depend on the problem's other dimensions (forward Y is bit-exact
+// between tiled and untiled runs).
+//
+// Every wait on an mbarrier is bounded (%globaltimer, 2 s).  On timeout the
+// thread ORs an error bit into *err and its role stops; the other roles see
+// the error word and stop too; the producer waits (time-bounded) for its own
+// TMA loads to land, the MMA thread for its own MMAs, and TMEM is freed
+// before the CTA exits.
+#include "tl_gemm.h"
+#include "tl_ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <mutex>
+
+namespace tl {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kUmmaK = 16;
+constexpr uint32_t kStageA = kBlockM * kBlockK * 2;  // 16 KiB
+constexpr uint32_t kStageB = kBlockN * kBlockK * 2;  // 32 KiB
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr uint32_t kMnChunk = 64 * kBlockK * 2;      // 64 MN elements x 64 K rows = 8 KiB
+constexpr uint32_t kTmemCols = 2 * kBlockN;          // two fp32 accumulators of 256 columns
+constexpr int kThreads = 256;
+constexpr int kFirstEpilogueWarp = 4;
+constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 256 + 1024;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kGroupM = 16;
+
+static_assert(kBlockK * 2 == 128, "one K-block row must be one 128-byte swizzle row");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct KParams {
+    int32_t m_dim, n_dim, k_dim;
+    int32_t num_m, num_n, num_k, num_tiles;
+    void* d;
+    int64_t ldd;
+    int32_t accumulate;
+    int32_t* err;
+};
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int32_t* err, int32_t code,
+                                       bool stop_on_error) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 255u) == 0) {
+            if (stop_on_error && *reinterpret_cast<volatile int32_t*>(err) != 0) return false;
+            if (global_timer_ns() - t0 > kTimeoutNs) {
+                atomicOr(err, code);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, int32_t* err,
+                                             int32_t code, bool stop_on_error = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, err, code, stop_on_error);
+}
+
+// Warp-uniform wait: lane 0 waits (bounded); then every lane observes the
+// completed phase itself, which cannot move on before this warp arrives.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t* err, int32_t code,
+                                          int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bounded(bar, parity, err, code) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) return false;
+    int mine = 0;
+    for (int n = 0; n < (1 << 20) && !mine; ++n) mine = mbar_try_wait(bar, parity) ? 1 : 0;
+    if (!mine) atomicOr(err, code);
+    return __all_sync(0xffffffffu, mine) != 0;
+}
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+    const int group_tiles = kGroupM * num_n;
+    const int g = tile / group_tiles;
+    const int first_m = g * kGroupM;
+    const int gm = min(kGroupM, num_m - first_m);
+    const int local = tile - g * group_tiles;
+    mb = first_m + local % gm;
+    nb = local / gm;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool OUT_F32>
+__device__ __forceinline__ void store_chunk(const KParams& p, int64_t row, int col,
+                                            const uint32_t (&v)[32]) {
+    const int rem = p.n_dim - col;
+    if constexpr (OUT_F32) {
+        float* out = static_cast<float*>(p.d) + row * p.ldd + col;
+        if (rem >= 32) {
+            float4* o = reinterpret_cast<float4*>(out);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float4 val = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                         __uint_as_float(v[4 * j + 2]),
+                                         __uint_as_float(v[4 * j + 3]));
+                if (p.accumulate) {
+                    const float4 old = o[j];
+                    val.x = old.x + val.x;
+                    val.y = old.y + val.y;
+                    val.z = old.z + val.z;
+                    val.w = old.w + val.w;
+                }
+                o[j] = val;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j < rem) {
+                    const float val = __uint_as_float(v[j]);
+                    out[j] = p.accumulate ? out[j] + val : val;
+                }
+            }
+        }
+    } else {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col;
+        if (rem >= 32) {
+            uint4* o = reinterpret_cast<uint4*>(out);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                o[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                                  pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                                  pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                                  pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < rem) out[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+    }
+}
+
+template <bool A_MN, bool B_MN, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t bar0 = smem_addr(bars);
+    const uint32_t smem0 = smem_addr(smem);
+    // barrier addresses: full[s], empty[s], tmem_full[a], tmem_empty[a], drain
+    auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        mbar_init_fence();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            tma_prefetch_map(&map_a);
+            tma_prefetch_map(&map_b);
+            uint32_t fills = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p.num_m, p.num_n, mb, nb);
+                const int m0 = mb * kBlockM, n0 = nb * kBlockN;
+                for (int kb = 0; kb < p.num_k; ++kb, ++fills) {
+                    const uint32_t s = fills % kStages;
+                    const uint32_t ph = (fills / kStages) & 1u;
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, p.err, kErrProducerWait)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem0 + s * kStageBytes;
+                    const uint32_t sb = sa + kStageA;
+                    const int k0 = kb * kBlockK;
+                    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+                    if (A_MN) {
+                        tma_load_2d(sa, &map_a, full_bar(s), m0, k0);
+                        tma_load_2d(sa + kMnChunk, &map_a, full_bar(s), m0 + 64, k0);
+                    } else {
+                        tma_load_2d(sa, &map_a, full_bar(s), k0, m0);
+                    }
+                    if (B_MN) {
+#pragma unroll
+                        for (int c = 0; c < kBlockN / 64; ++c)
+                            tma_load_2d(sb + c * kMnChunk, &map_b, full_bar(s), n0 + 64 * c, k0);
+                    } else {
+                        tma_load_2d(sb, &map_b, full_bar(s), k0, n0);
+                    }
+                }
+            }
+            // Our own loads must land before the CTA may exit.
+            const uint32_t outstanding = fills < uint32_t(kStages) ? fills : uint32_t(kStages);
+            for (uint32_t j = 0; j < outstanding; ++j) {
+                const uint32_t f = fills - 1 - j;
+                wait_bounded(full_bar(f % kStages), (f / kStages) & 1u, p.err, kErrDrainWait, false);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, A_MN, B_MN);
+            uint32_t fills = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+                const uint32_t acc = it & 1;
+                const uint32_t acc_ph = (it >> 1) & 1;
+                if (!wait_bounded(tempty_bar(acc), acc_ph ^ 1u, p.err, kErrMmaWaitTmem)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kBlockN;
+                for (int kb = 0; kb < p.num_k; ++kb, ++fills) {
+                    const uint32_t s = fills % kStages;
+                    const uint32_t ph = (fills / kStages) & 1u;
+                    if (!wait_bounded(full_bar(s), ph, p.err, kErrMmaWaitFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem0 + s * kStageBytes;
+                    const uint32_t sb = sa + kStageA;
+#pragma unroll
+                    for (int j = 0; j < kBlockK / kUmmaK; ++j) {
+                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + j * 2048, kMnChunk, 1024)
+                                                 : smem_desc_sw128(sa + j * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + j * 2048, kMnChunk, 1024)
+                                                 : smem_desc_sw128(sb + j * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(s));
+                }
+                if (ok) umma_commit(tfull_bar(acc));
+            }
+            // Our own MMAs must complete before TMEM is freed.
+            umma_commit(drain_bar);
+            wait_bounded(drain_bar, 0, p.err, kErrDrainWait, false);
+        }
+    } else if (warp >= kFirstEpilogueWarp) {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int it = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+            const uint32_t acc = it & 1;
+            const uint32_t acc_ph = (it >> 1) & 1;
+            if (!warp_wait(tfull_bar(acc), acc_ph, p.err, kErrEpilogueWait, lane)) break;
+            tc_fence_after();
+            int mb, nb;
+            tile_coords(tile, p.num_m, p.num_n, mb, nb);
+            const int64_t row = int64_t(mb) * kBlockM + q * 32 + lane;
+            const int n0 = nb * kBlockN;
+            const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * kBlockN;
+            for (int c = 0; c < kBlockN; c += 32) {
+                if (n0 + c >= p.n_dim) break;  // warp-uniform
+                uint32_t v[32];
+                tmem_ld_32cols(t_row + c, v);
+                tmem_ld_wait();
+                if (row < p.m_dim) store_chunk<OUT_F32>(p, row, n0 + c, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows
+// `ld` elements apart, box of 64 x box_outer, 128-byte swizzle, zero fill
+// outside the tensor.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+              uint32_t box_outer, std::string* why) {
+    auto fn = encode_fn();
+    if (!fn) {
+        if (why) *why = "cuTensorMapEncodeTiled is unavailable from the driver";
+        return false;
+    }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (why) *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(int(r));
+        return false;
+    }
+    return true;
+}
+
+template <bool A_MN, bool B_MN, bool OUT_F32>
+cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp, int grid,
+                       cudaStream_t stream) {
+    auto kern = gemm_kernel<A_MN, B_MN, OUT_F32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, kp);
+    return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+std::string gemm_check(const GemmDesc& g) {
+    if (g.m_dim < 1 || g.n_dim < 1 || g.k_dim < 1) return "GEMM sizes must be >= 1";
+    if (g.m_dim > INT32_MAX / 2 || g.n_dim > INT32_MAX / 2 || g.k_dim > INT32_MAX / 2)
+        return "GEMM size too large";
+    if (!g.a || !g.b || !g.d || !g.err) return "null pointer";
+    if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.d))
+        return "operand pointers must be 16-byte aligned";
+    if (reinterpret_cast<uintptr_t>(g.err) & 3u) return "err pointer must be 4-byte aligned";
+    if (g.lda % 8 || g.ldb % 8 || g.ldd % 8)
+        return "leading dimensions must be multiples of 8 elements";
+    if ((g.a_mn_major ? g.m_dim : g.k_dim) > g.lda) return "A leading dimension too small";
+    if ((g.b_mn_major ? g.n_dim : g.k_dim) > g.ldb) return "B leading dimension too small";
+    if (g.n_dim > g.ldd) return "D leading dimension too small";
+    if (g.lda * 2 >= (int64_t(1) << 40) || g.ldb * 2 >= (int64_t(1) << 40))
+        return "leading dimension too large";
+    const int64_t tiles = ((g.m_dim + kBlockM - 1) / kBlockM) * ((g.n_dim + kBlockN - 1) / kBlockN);
+    if (tiles > INT32_MAX) return "too many output tiles";
+    const bool fwd = !g.a_mn_major && g.b_mn_major && g.out == OutKind::BF16;
+    const bool dw = g.a_mn_major && g.b_mn_major && g.out == OutKind::BF16;
+    const bool dx = !g.a_mn_major && !g.b_mn_major && g.out == OutKind::F32;
+    if (!(fwd || dw || dx)) return "unsupported operand-major / output combination";
+    if (g.accumulate && g.out != OutKind::F32) return "accumulate needs fp32 output";
+    return {};
+}
+
+cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std::string* why) {
+    std::string bad = gemm_check(g);
+    if (!bad.empty()) {
+        if (why) *why = bad;
+        return cudaErrorInvalidValue;
+    }
+    CUtensorMap ma, mb;
+    const bool ok_a = g.a_mn_major ? make_map(&ma, g.a, g.m_dim, g.k_dim, g.lda, 64, why)
+                                   : make_map(&ma, g.a, g.k_dim, g.m_dim, g.lda, kBlockM, why);
+    if (!ok_a) return cudaErrorInvalidValue;
+    const bool ok_b = g.b_mn_major ? make_map(&mb, g.b, g.n_dim, g.k_dim, g.ldb, 64, why)
+                                   : make_map(&mb, g.b, g.k_dim, g.n_dim, g.ldb, kBlockN, why);
+    if (!ok_b) return cudaErrorInvalidValue;
+
+    KParams kp{};
+    kp.m_dim = int32_t(g.m_dim);
+    kp.n_dim = int32_t(g.n_dim);
+    kp.k_dim = int32_t(g.k_dim);
+    kp.num_m = int32_t((g.m_dim + kBlockM - 1) / kBlockM);
+    kp.num_n = int32_t((g.n_dim + kBlockN - 1) / kBlockN);
+    kp.num_k = int32_t((g.k_dim + kBlockK - 1) / kBlockK);
+    kp.num_tiles = kp.num_m * kp.num_n;
+    kp.d = g.d;
+    kp.ldd = g.ldd;
+    kp.accumulate = g.accumulate ? 1 : 0;
+    kp.err = g.err;
+    const int grid = kp.num_tiles < num_sms ? kp.num_tiles : num_sms;
+
+    cudaError_t e;
+    if (!g.a_mn_major && g.b_mn_major)
+        e = launch_one<false, true, false>(ma, mb, kp, grid, stream);
+    else if (g.a_mn_major && g.b_mn_major)
+        e = launch_one<true, true, false>(ma, mb, kp, grid, stream);
+    else
+        e = launch_one<false, false, true>(ma, mb, kp, grid, stream);
+    if (e != cudaSuccess && why) *why = std::string("kernel launch: ") + cudaGetErrorString(e);
+    return e;
+}
+
+}  // namespace tl

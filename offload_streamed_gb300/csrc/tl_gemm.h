@@ -1,0 +1,58 @@
+// tl_gemm.h -- internal interface of the three tile GEMMs (host side).
+//
+//   forward  (K1): Y_i  = X . W_i          A = X  (K-major), B = W_i (N-major)
+//   weight   (K3): dW_i = X^T . dY_i       A = X^T (M-major), B = dY_i (N-major)
+//   input    (K2): dX  (+)= dY_i . W_i^T   A = dY_i (K-major), B = W_i^T (K-major)
+//
+// All three run one persistent kernel template: bf16 operands fed by TMA into
+// a shared-memory ring, tcgen05 MMAs accumulating in fp32 in tensor memory,
+// and an epilogue that rounds to bf16 (K1, K3) or stores / adds fp32 (K2).
+#pragma once
+#include <cstdint>
+#include <string>
+#include <cuda_runtime.h>
+
+namespace tl {
+
+enum class OutKind : int { BF16 = 0, F32 = 1 };
+
+// D[m_dim, n_dim] (ld ldd) = sum_k A[m, k] B[k, n] over k < k_dim.
+// A is given either K-major (a_ptr[m * lda + k]) or M-major (a_ptr[k * lda + m]);
+// B either K-major (b_ptr[n * ldb + k]) or N-major (b_ptr[k * ldb + n]).
+struct GemmDesc {
+    int64_t m_dim = 0, n_dim = 0, k_dim = 0;
+    const void* a = nullptr;
+    int64_t lda = 0;
+    bool a_mn_major = false;
+    const void* b = nullptr;
+    int64_t ldb = 0;
+    bool b_mn_major = false;
+    void* d = nullptr;
+    int64_t ldd = 0;
+    OutKind out = OutKind::BF16;
+    bool accumulate = false;  // F32 only: D += A.B
+    int32_t* err = nullptr;   // device word for bounded-wait timeouts
+};
+
+// Shape / alignment rules shared by the launcher and the ABI checks.
+// Returns an empty string if `g` can be launched, else the reason.
+std::string gemm_check(const GemmDesc& g);
+
+// Enqueue one GEMM on `stream`.  num_sms = persistent grid bound.
+cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std::string* why);
+
+// Tile shape of the kernel (exported for sizing and tests).
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 256;
+constexpr int kBlockK = 64;
+
+// Error bits a kernel ORs into *err when a bounded wait gives up.
+enum : int32_t {
+    kErrProducerWait = 1,
+    kErrMmaWaitFull = 2,
+    kErrMmaWaitTmem = 4,
+    kErrEpilogueWait = 8,
+    kErrDrainWait = 16,
+};
+
+}  // namespace tl

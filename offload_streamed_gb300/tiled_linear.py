@@ -1,0 +1,274 @@
+"""Python binding of ``libtiled_linear.so`` (the C ABI in ``include/tiled_linear.h``).
+
+Argument marshalling only: every step of the forward / backward path runs in
+the library's CUDA kernels and copy streams.  There is no fallback: if the
+shared library is missing or fails to load, every entry point raises.
+
+Module-level functions carry the C names and take plain integers (pointers,
+sizes, stream handles).  ``TiledLinear`` and ``PinnedBuffer`` wrap them for
+PyTorch callers: PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+TL_OK, TL_ERR_INVALID, TL_ERR_NOT_PINNED, TL_ERR_WORKSPACE, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_STATE = range(7)
+STATUS_NAMES = {0: "TL_OK", 1: "TL_ERR_INVALID", 2: "TL_ERR_NOT_PINNED", 3: "TL_ERR_WORKSPACE",
+                4: "TL_ERR_CUDA", 5: "TL_ERR_TIMEOUT", 6: "TL_ERR_STATE"}
+
+
+class TiledLinearError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}"
+                         + (f" ({message})" if message else ""))
+
+
+class tl_stats(ctypes.Structure):
+    _fields_ = [
+        ("n_tiles", ctypes.c_int32), ("depth", ctypes.c_int32),
+        ("fwd_valid", ctypes.c_int32), ("bwd_valid", ctypes.c_int32),
+        ("fwd_total_ms", ctypes.c_float), ("fwd_gemm_ms", ctypes.c_float), ("fwd_h2d_ms", ctypes.c_float),
+        ("bwd_total_ms", ctypes.c_float), ("bwd_dw_gemm_ms", ctypes.c_float),
+        ("bwd_dx_gemm_ms", ctypes.c_float), ("bwd_h2d_ms", ctypes.c_float), ("bwd_d2h_ms", ctypes.c_float),
+        ("fwd_wait_ms", ctypes.c_float), ("bwd_wait_ms", ctypes.c_float),
+        ("fwd_h2d_bytes", ctypes.c_int64), ("bwd_h2d_bytes", ctypes.c_int64), ("bwd_d2h_bytes", ctypes.c_int64),
+        ("fwd_launches", ctypes.c_int32), ("bwd_launches", ctypes.c_int32),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load the shared library (it must have been built: ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(path)
+        i64, i32, sz, vp, st = ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
+        L.tiled_linear_workspace_bytes.argtypes = [i64, i64, i32, i32]
+        L.tiled_linear_workspace_bytes.restype = sz
+        for name in ("tiled_linear_create", "tiled_linear_create_tilemajor"):
+            fn = getattr(L, name)
+            fn.argtypes = [ctypes.POINTER(vp), i64, i64, i32, i32, vp, vp, vp, sz, ctypes.c_int]
+            fn.restype = st
+        L.tiled_linear_forward.argtypes = [vp, i64, vp, vp, vp]
+        L.tiled_linear_forward.restype = st
+        L.tiled_linear_backward.argtypes = [vp, i64, vp, vp, vp, vp]
+        L.tiled_linear_backward.restype = st
+        L.tiled_linear_destroy.argtypes = [vp]
+        L.tiled_linear_destroy.restype = st
+        L.tiled_linear_last_error.argtypes = [vp]
+        L.tiled_linear_last_error.restype = ctypes.c_char_p
+        L.tiled_linear_get_stats.argtypes = [vp, vp]
+        L.tiled_linear_get_stats.restype = st
+        L.tiled_linear_gemm_forward.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp]
+        L.tiled_linear_gemm_forward.restype = st
+        L.tiled_linear_gemm_dw.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp]
+        L.tiled_linear_gemm_dw.restype = st
+        L.tiled_linear_gemm_dx.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp, vp]
+        L.tiled_linear_gemm_dx.restype = st
+        L.tiled_linear_host_alloc.argtypes = [sz, ctypes.POINTER(vp)]
+        L.tiled_linear_host_alloc.restype = st
+        L.tiled_linear_host_free.argtypes = [vp]
+        L.tiled_linear_host_free.restype = st
+        L.tiled_linear_version.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def _check(status: int, where: str, handle=None):
+    if status != TL_OK:
+        raise TiledLinearError(status, where, tiled_linear_last_error(handle))
+
+
+# --- the C ABI, name for name ----------------------------------------------
+
+def tiled_linear_workspace_bytes(K: int, M: int, N: int, d: int) -> int:
+    return int(load().tiled_linear_workspace_bytes(K, M, N, d))
+
+
+def tiled_linear_create(K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes, device,
+                        tile_major: bool = False) -> int:
+    """Returns the handle (an integer).  ``tile_major`` selects
+    ``tiled_linear_create_tilemajor``."""
+    h = ctypes.c_void_p()
+    fn = load().tiled_linear_create_tilemajor if tile_major else load().tiled_linear_create
+    _check(fn(ctypes.byref(h), K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes, device),
+           "tiled_linear_create")
+    return h.value
+
+
+def tiled_linear_create_tilemajor(K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes,
+                                  device) -> int:
+    return tiled_linear_create(K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes, device,
+                               tile_major=True)
+
+
+def tiled_linear_forward(h: int, T: int, x_dev: int, y_dev: int, stream: int) -> None:
+    _check(load().tiled_linear_forward(h, T, x_dev, y_dev, stream), "tiled_linear_forward", h)
+
+
+def tiled_linear_backward(h: int, T: int, x_dev: int, dy_dev: int, dx_dev: int, stream: int) -> None:
+    _check(load().tiled_linear_backward(h, T, x_dev, dy_dev, dx_dev, stream), "tiled_linear_backward", h)
+
+
+def tiled_linear_destroy(h: int) -> int:
+    return int(load().tiled_linear_destroy(h))
+
+
+def tiled_linear_last_error(h=None) -> str:
+    msg = load().tiled_linear_last_error(h)
+    return msg.decode(errors="replace") if msg else ""
+
+
+def tiled_linear_get_stats(h: int) -> dict:
+    s = tl_stats()
+    _check(load().tiled_linear_get_stats(h, ctypes.byref(s)), "tiled_linear_get_stats", h)
+    return s.as_dict()
+
+
+def tiled_linear_gemm_forward(T, K, n, x, ldx, w, ldw, y, ldy, err, stream) -> None:
+    _check(load().tiled_linear_gemm_forward(T, K, n, x, ldx, w, ldw, y, ldy, err, stream),
+           "tiled_linear_gemm_forward")
+
+
+def tiled_linear_gemm_dw(T, K, n, x, ldx, dy, lddy, dw, lddw, err, stream) -> None:
+    _check(load().tiled_linear_gemm_dw(T, K, n, x, ldx, dy, lddy, dw, lddw, err, stream),
+           "tiled_linear_gemm_dw")
+
+
+def tiled_linear_gemm_dx(T, K, n, dy, lddy, w, ldw, dx, lddx, accumulate, err, stream) -> None:
+    _check(load().tiled_linear_gemm_dx(T, K, n, dy, lddy, w, ldw, dx, lddx, int(accumulate), err, stream),
+           "tiled_linear_gemm_dx")
+
+
+def tiled_linear_host_alloc(nbytes: int) -> int:
+    p = ctypes.c_void_p()
+    _check(load().tiled_linear_host_alloc(nbytes, ctypes.byref(p)), "tiled_linear_host_alloc")
+    return p.value
+
+
+def tiled_linear_host_free(p: int) -> None:
+    _check(load().tiled_linear_host_free(p), "tiled_linear_host_free")
+
+
+def tiled_linear_version() -> str:
+    return load().tiled_linear_version().decode()
+
+
+# --- PyTorch convenience wrappers --------------------------------------------
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class PinnedBuffer:
+    """Page-locked host memory from ``tiled_linear_host_alloc``, viewed as a
+    CPU tensor of ``dtype``.  Freed by ``close()`` (or garbage collection)."""
+
+    def __init__(self, numel: int, dtype=None):
+        import torch
+        from .inputs import host_tensor
+        self.dtype = dtype or torch.bfloat16
+        self.numel = int(numel)
+        itemsize = torch.empty((), dtype=self.dtype).element_size()
+        self.nbytes = self.numel * itemsize
+        self.ptr = tiled_linear_host_alloc(max(self.nbytes, 16))
+        self.tensor = host_tensor(self.ptr, self.numel, self.dtype)
+
+    def close(self):
+        if self.ptr:
+            self.tensor = None
+            tiled_linear_host_free(self.ptr)
+            self.ptr = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class TiledLinear:
+    """Y = X.W with W [K, M] in pinned host memory, streamed in N output tiles
+    through a depth-d device ring (see ``include/tiled_linear.h``).
+
+    w_host / dw_host: pinned host buffers (``PinnedBuffer`` or a pinned CPU
+    tensor) of K*M bf16 each, tile-major [N][K][M/N] when ``tile_major`` else
+    row-major [K][M].  The workspace is a device uint8 tensor owned here."""
+
+    def __init__(self, K: int, M: int, N: int, d: int, w_host, dw_host, *, tile_major: bool = True,
+                 device=None):
+        import torch
+        self.K, self.M, self.N, self.d = int(K), int(M), int(N), int(d)
+        self.Mi = self.M // self.N
+        self.tile_major = bool(tile_major)
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
+                                   torch.device(device).index or 0)
+        wb = tiled_linear_workspace_bytes(self.K, self.M, self.N, self.d)
+        if wb == 0:
+            raise TiledLinearError(TL_ERR_INVALID, "tiled_linear_workspace_bytes",
+                                   f"invalid shape K={K} M={M} N={N} d={d}")
+        self.workspace = torch.empty(wb, dtype=torch.uint8, device=self.device)
+        self._w, self._dw = w_host, dw_host
+        wp = w_host.ptr if isinstance(w_host, PinnedBuffer) else w_host.data_ptr()
+        dwp = dw_host.ptr if isinstance(dw_host, PinnedBuffer) else dw_host.data_ptr()
+        self.handle = tiled_linear_create(self.K, self.M, self.N, self.d, wp, dwp,
+                                          self.workspace.data_ptr(), wb, self.device.index,
+                                          tile_major=self.tile_major)
+
+    def forward(self, x, y=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty(T, self.M, dtype=torch.bfloat16, device=self.device)
+        tiled_linear_forward(self.handle, T, x.data_ptr(), y.data_ptr(), _stream_handle(stream))
+        return y
+
+    def backward(self, x, dy, dx=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if dx is None:
+            dx = torch.empty(T, self.K, dtype=torch.float32, device=self.device)
+        tiled_linear_backward(self.handle, T, x.data_ptr(), dy.data_ptr(), dx.data_ptr(),
+                              _stream_handle(stream))
+        return dx
+
+    def stats(self) -> dict:
+        return tiled_linear_get_stats(self.handle)
+
+    def close(self) -> int:
+        st = TL_OK
+        if self.handle:
+            st = tiled_linear_destroy(self.handle)
+            self.handle = 0
+        return st
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

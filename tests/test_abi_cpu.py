@@ -1,0 +1,110 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, sizes workspaces as the closed forms say, and rejects bad arguments
+before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import closed_forms as CF
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tiled_linear.h")
+
+
+@pytest.fixture(scope="module")
+def tl():
+    from offload_streamed_gb300 import _build
+    _build.build()
+    from offload_streamed_gb300 import tiled_linear
+    tiled_linear.load()
+    return tiled_linear
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tiled_linear_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("tiled_linear_create", "tiled_linear_forward", "tiled_linear_backward",
+                     "tiled_linear_destroy", "tiled_linear_workspace_bytes",
+                     "tiled_linear_last_error", "tiled_linear_get_stats"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(tl):
+    lib = ctypes.CDLL(tl.lib_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_has_the_same_names(tl):
+    for n in declared_functions():
+        assert callable(getattr(tl, n, None)), n
+
+
+def test_version(tl):
+    assert "sm_103a" in tl.tiled_linear_version()
+
+
+@pytest.mark.parametrize("K,M,N,d", [(1024, 4096, 4, 1), (8192, 32768, 8, 2), (25600, 102400, 16, 3),
+                                     (65536, 262144, 16, 2), (16384, 65536, 16, 4), (64, 64, 1, 0),
+                                     (1024, 4096, 4, 9)])
+def test_workspace_bytes_matches_closed_form(tl, K, M, N, d):
+    tile = CF.tile_bytes(K, M, N)
+    tile_al = (tile + 255) // 256 * 256
+    ring = CF.ring_bytes(K, M, N, d) // tile * tile_al
+    staging = min(2, N) * tile_al
+    assert tl.tiled_linear_workspace_bytes(K, M, N, d) == 4096 + ring + staging
+
+
+def test_workspace_bytes_auto_depth(tl):
+    tile = CF.tile_bytes(1024, 4096, 4)
+    assert tl.tiled_linear_workspace_bytes(1024, 4096, 4, -1) == 4096 + (4 + 2) * tile
+    assert tl.tiled_linear_workspace_bytes(1024, 4096 * 4, 16, -1) == 4096 + (4 + 2) * tile
+
+
+@pytest.mark.parametrize("K,M,N,d", [(0, 64, 1, 0), (12, 64, 1, 0), (64, 65, 1, 0), (64, 64, 3, 0),
+                                     (64, 100, 2, 0), (64, 64, 0, 0), (64, 64, 1, -2)])
+def test_invalid_shapes(tl, K, M, N, d):
+    assert tl.tiled_linear_workspace_bytes(K, M, N, d) == 0
+    with pytest.raises(tl.TiledLinearError) as ei:
+        tl.tiled_linear_create(K, M, N, d, 16, 16, 256, 1 << 30, 0)
+    assert ei.value.status == tl.TL_ERR_INVALID
+    assert tl.tiled_linear_last_error(None)
+
+
+def test_null_pointers_and_small_workspace(tl):
+    with pytest.raises(tl.TiledLinearError) as ei:
+        tl.tiled_linear_create(64, 64, 1, 0, 0, 16, 256, 1 << 20, 0)
+    assert ei.value.status == tl.TL_ERR_INVALID
+    need = tl.tiled_linear_workspace_bytes(64, 64, 1, 0)
+    with pytest.raises(tl.TiledLinearError) as ei:
+        tl.tiled_linear_create(64, 64, 1, 0, 16, 16, 256, need - 1, 0)
+    assert ei.value.status == tl.TL_ERR_WORKSPACE
+    with pytest.raises(tl.TiledLinearError) as ei:  # misaligned workspace
+        tl.tiled_linear_create(64, 64, 1, 0, 16, 16, 256 + 16, need, 0)
+    assert ei.value.status == tl.TL_ERR_WORKSPACE
+
+
+def test_null_handle_calls(tl):
+    lib = tl.load()
+    assert lib.tiled_linear_forward(None, 1, None, None, None) == tl.TL_ERR_STATE
+    assert lib.tiled_linear_backward(None, 1, None, None, None, None) == tl.TL_ERR_STATE
+    assert lib.tiled_linear_destroy(None) == tl.TL_OK
+    assert lib.tiled_linear_get_stats(None, None) == tl.TL_ERR_INVALID
+
+
+def test_resident_gemm_argument_checks(tl):
+    lib = tl.load()
+    # sizes < 1, null pointers and unaligned leading dimensions are refused
+    # before any CUDA call
+    assert lib.tiled_linear_gemm_forward(0, 64, 64, 256, 64, 256, 64, 256, 64, 256, None) == tl.TL_ERR_INVALID
+    assert lib.tiled_linear_gemm_forward(64, 64, 64, None, 64, 256, 64, 256, 64, 256, None) == tl.TL_ERR_INVALID
+    assert lib.tiled_linear_gemm_dw(64, 64, 64, 256, 60, 256, 64, 256, 64, 256, None) == tl.TL_ERR_INVALID
+    assert lib.tiled_linear_gemm_dx(64, 64, 64, 256, 64, 256, 64, 256, 32, 0, 256, None) == tl.TL_ERR_INVALID
+    assert lib.tiled_linear_gemm_dx(64, 64, 64, 258, 64, 256, 64, 256, 64, 0, 256, None) == tl.TL_ERR_INVALID
