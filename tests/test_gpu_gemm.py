@@ -44,7 +44,8 @@ def test_gemm_forward(tl, T, K, n):
     y = torch.empty(T, n, dtype=torch.bfloat16, device="cuda")
     err = _err_word()
     s = torch.cuda.current_stream()
-    tl.tiled_linear_gemm_forward(T, K, n, _dev(x).data_ptr(), K, (wd := _dev(w)).data_ptr(), n,
+    xd, wd = _dev(x), _dev(w)  # keep the device copies alive until the kernel is done
+    tl.tiled_linear_gemm_forward(T, K, n, xd.data_ptr(), K, wd.data_ptr(), n,
                                  y.data_ptr(), n, err.data_ptr(), s.cuda_stream)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
@@ -52,7 +53,6 @@ def test_gemm_forward(tl, T, K, n):
     ref = O.forward(xb, wb)
     S = np.abs(bf16_bits_to_f64(xb)) @ np.abs(bf16_bits_to_f64(wb))
     check("Y", y.float().cpu().numpy(), ref, S, K, bf16_out=True)
-    del wd
 
 
 @pytest.mark.parametrize("T,K,n", SHAPES)
