@@ -61,10 +61,13 @@ typedef enum {
  *              1-D copies, which keep the full host-link bandwidth). */
 typedef enum { TL_LAYOUT_ROW_MAJOR = 0, TL_LAYOUT_TILE_MAJOR = 1 } tl_layout;
 
-/* Per-call timings, from CUDA events the library records on the streams that
- * run the work.  Times in milliseconds; *_gemm_ms are sums over the tiles of
- * the kernel's own span on the compute stream; *_copy_ms are sums of the copy
- * spans on the copy streams; *_total_ms spans the whole call on `stream`. */
+/* Timings from CUDA events the library records on the streams that run the
+ * work, in milliseconds.  The first block describes the LAST forward and
+ * backward call: *_gemm_ms are sums over the tiles of each kernel's own span
+ * on the compute stream, *_h2d_ms / *_d2h_ms sums of the copy spans on the
+ * copy streams, *_total_ms the whole call on `stream`.  The sum_* block adds
+ * the same quantities over every call since the handle was created or
+ * tiled_linear_reset_stats was called (fwd_calls / bwd_calls of them). */
 typedef struct {
     int32_t n_tiles;
     int32_t depth;            /* d used by the call                           */
@@ -75,6 +78,9 @@ typedef struct {
     float bwd_wait_ms;        /* bwd_total - both GEMM sums                   */
     int64_t fwd_h2d_bytes, bwd_h2d_bytes, bwd_d2h_bytes;
     int32_t fwd_launches, bwd_launches;   /* kernels launched by the call     */
+    int64_t fwd_calls, bwd_calls;
+    double sum_fwd_total_ms, sum_fwd_gemm_ms, sum_fwd_h2d_ms;
+    double sum_bwd_total_ms, sum_bwd_dw_gemm_ms, sum_bwd_dx_gemm_ms, sum_bwd_h2d_ms, sum_bwd_d2h_ms;
 } tl_stats;
 
 /* Device workspace bytes needed for (K, M, N, d): (min(d,N-1)+1) weight slots
@@ -140,6 +146,9 @@ const char *tiled_linear_last_error(const tl_handle *h);
  * kernels' timeout word, and fill *out (a tl_stats).  Returns TL_ERR_TIMEOUT
  * if a kernel gave up waiting. */
 tl_status tiled_linear_get_stats(tl_handle *h, void *tl_stats_out);
+
+/* Wait for every recorded call to finish and zero the sum_* counters. */
+tl_status tiled_linear_reset_stats(tl_handle *h);
 
 /* --- resident GEMMs: the three kernels on device-resident operands --------
  * The same kernels the engine launches per tile, for callers that already

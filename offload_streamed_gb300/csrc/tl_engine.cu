@@ -67,15 +67,31 @@ int32_t slots_for(int32_t N, int32_t d) {
 
 size_t tile_bytes(int64_t K, int64_t Mi) { return size_t(K) * size_t(Mi) * 2; }
 
-struct CallTiming {
-    bool valid = false;
+constexpr int kTimingRing = 16;
+
+// Timing events of one call.  Per tile: [0] kernel-1 start, [1] kernel-1 end,
+// [2] kernel-2 start, [3] kernel-2 end, [4] h2d start, [5] h2d end, [6] d2h
+// start, [7] d2h end.  Forward records [0],[1],[4],[5].
+struct CallSlot {
     cudaEvent_t start = nullptr, end = nullptr;
-    // per tile: [0] kernel-1 start, [1] kernel-1 end, [2] kernel-2 start,
-    // [3] kernel-2 end, [4] h2d start, [5] h2d end, [6] d2h start, [7] d2h end
     std::vector<cudaEvent_t> ev[8];
-    int32_t depth = 0;
-    int32_t launches = 0;
+    bool pending = false;  // recorded, not yet harvested
+    bool harvested = false;
+    int32_t depth = 0, launches = 0;
     int64_t h2d_bytes = 0, d2h_bytes = 0;
+    float total = 0, gemm1 = 0, gemm2 = 0, h2d = 0, d2h = 0;
+};
+
+// A ring of call slots: a call reuses the slot of the call kTimingRing
+// earlier, harvesting its timings first (that call finished long ago, so the
+// host does not stall the device).  Harvested calls are added to the sums.
+struct Phase {
+    bool backward = false;
+    std::vector<CallSlot> ring;
+    uint64_t calls = 0;
+    int last = -1;
+    int64_t sum_calls = 0;
+    double sum_total = 0, sum_gemm1 = 0, sum_gemm2 = 0, sum_h2d = 0, sum_d2h = 0;
 };
 
 }  // namespace
@@ -97,7 +113,7 @@ struct tl_handle {
     std::vector<cudaEvent_t> ev_ready, ev_free, ev_dwdone, ev_drained;
     uint64_t fetch_seq = 0, stage_seq = 0;
     int num_sms = 0;
-    CallTiming fwd, bwd;
+    Phase fwd, bwd;
     tl_status sticky = TL_OK;
     std::string msg;
 };
@@ -149,22 +165,30 @@ bool is_device_mem(const void* p, int device) {
     return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == device;
 }
 
-tl_status create_events(tl_handle* h, CallTiming& t, int n) {
-    TL_TRY(h, cudaEventCreate(&t.start));
-    TL_TRY(h, cudaEventCreate(&t.end));
-    for (auto& v : t.ev) {
-        v.assign(size_t(n), nullptr);
-        for (auto& e : v) TL_TRY(h, cudaEventCreate(&e));
+tl_status create_phase(tl_handle* h, Phase& p, int n, bool backward) {
+    p.backward = backward;
+    p.ring.resize(kTimingRing);
+    for (auto& c : p.ring) {
+        TL_TRY(h, cudaEventCreate(&c.start));
+        TL_TRY(h, cudaEventCreate(&c.end));
+        for (int k = 0; k < 8; ++k) {
+            if (!backward && (k == 2 || k == 3 || k == 6 || k == 7)) continue;
+            c.ev[k].assign(size_t(n), nullptr);
+            for (auto& e : c.ev[k]) TL_TRY(h, cudaEventCreate(&e));
+        }
     }
     return TL_OK;
 }
 
-void destroy_events(CallTiming& t) {
-    if (t.start) cudaEventDestroy(t.start);
-    if (t.end) cudaEventDestroy(t.end);
-    for (auto& v : t.ev)
-        for (auto e : v)
-            if (e) cudaEventDestroy(e);
+void destroy_phase(Phase& p) {
+    for (auto& c : p.ring) {
+        if (c.start) cudaEventDestroy(c.start);
+        if (c.end) cudaEventDestroy(c.end);
+        for (auto& v : c.ev)
+            for (auto e : v)
+                if (e) cudaEventDestroy(e);
+    }
+    p.ring.clear();
 }
 
 // Read the pinned mirror of the kernels' error word (written at the end of
@@ -220,18 +244,61 @@ float span_ms(cudaEvent_t a, cudaEvent_t b) {
     return ms;
 }
 
+tl_status harvest(tl_handle* h, Phase& p, CallSlot& c, int n) {
+    if (!c.pending) return TL_OK;
+    TL_TRY(h, cudaEventSynchronize(c.end));
+    c.total = span_ms(c.start, c.end);
+    c.gemm1 = c.gemm2 = c.h2d = c.d2h = 0;
+    for (int i = 0; i < n; ++i) {
+        c.gemm1 += span_ms(c.ev[0][i], c.ev[1][i]);
+        c.h2d += span_ms(c.ev[4][i], c.ev[5][i]);
+        if (p.backward) {
+            c.gemm2 += span_ms(c.ev[2][i], c.ev[3][i]);
+            c.d2h += span_ms(c.ev[6][i], c.ev[7][i]);
+        }
+    }
+    c.pending = false;
+    c.harvested = true;
+    p.sum_calls += 1;
+    p.sum_total += c.total;
+    p.sum_gemm1 += c.gemm1;
+    p.sum_gemm2 += c.gemm2;
+    p.sum_h2d += c.h2d;
+    p.sum_d2h += c.d2h;
+    return TL_OK;
+}
+
+tl_status harvest_all(tl_handle* h, Phase& p) {
+    for (auto& c : p.ring) {
+        tl_status st = harvest(h, p, c, h->s.N);
+        if (st != TL_OK) return st;
+    }
+    return TL_OK;
+}
+
+// Slot for the next call of phase p (harvesting the call that used it last).
+CallSlot* begin_call(tl_handle* h, Phase& p, tl_status* st) {
+    CallSlot& c = p.ring[p.calls % kTimingRing];
+    *st = harvest(h, p, c, h->s.N);
+    return *st == TL_OK ? &c : nullptr;
+}
+
+void end_call(Phase& p, CallSlot& c) {
+    c.pending = true;
+    c.harvested = false;
+    p.last = int(p.calls % kTimingRing);
+    p.calls += 1;
+}
+
 // Automatic depth: after the first forward call, d = ceil(t_fetch / t_layer)
 // from that call's measured copy and kernel spans (tm_zero_infinity,
 // "Prefetch depth"), bounded by the slots the workspace holds.
 tl_status finish_auto_depth(tl_handle* h) {
-    if (!h->auto_pending || !h->fwd.valid) return TL_OK;
-    TL_TRY(h, cudaEventSynchronize(h->fwd.end));
-    const int n = h->s.N;
-    double fetch = 0, layer = 0;
-    for (int i = 0; i < n; ++i) {
-        fetch += span_ms(h->fwd.ev[4][i], h->fwd.ev[5][i]);
-        layer += span_ms(h->fwd.ev[0][i], h->fwd.ev[1][i]);
-    }
+    if (!h->auto_pending || h->fwd.last < 0) return TL_OK;
+    CallSlot& c = h->fwd.ring[h->fwd.last];
+    tl_status st = harvest(h, h->fwd, c, h->s.N);
+    if (st != TL_OK) return st;
+    const double fetch = c.h2d, layer = c.gemm1;
     int32_t dnew = 1;
     if (layer > 0) dnew = int32_t(std::ceil(fetch / layer));
     dnew = std::max<int32_t>(1, std::min<int32_t>(dnew, h->slot_cap - 1));
@@ -347,7 +414,7 @@ tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t 
         h->msg = std::string("event creation: ") + cudaGetErrorString(cudaGetLastError());
         return bail(TL_ERR_CUDA);
     }
-    if (create_events(h, h->fwd, N) != TL_OK || create_events(h, h->bwd, N) != TL_OK)
+    if (create_phase(h, h->fwd, N, false) != TL_OK || create_phase(h, h->bwd, N, true) != TL_OK)
         return bail(TL_ERR_CUDA);
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
         h->msg = "cudaDeviceGetAttribute(multiProcessorCount) failed";
@@ -395,7 +462,9 @@ tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void*
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const Shape& s = h->s;
-    CallTiming& t = h->fwd;
+    CallSlot* tp = begin_call(h, h->fwd, &st);
+    if (!tp) return st;
+    CallSlot& t = *tp;
     const int nslots = h->d + 1;
     TL_TRY(h, cudaEventRecord(t.start, cs));
     for (int i = 0; i < s.N; ++i) {
@@ -428,11 +497,11 @@ tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void*
     }
     TL_TRY(h, cudaEventRecord(t.end, cs));
     TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
-    t.valid = true;
     t.depth = h->d;
     t.launches = s.N;
     t.h2d_bytes = int64_t(s.N) * int64_t(tile_bytes(s.K, s.Mi));
     t.d2h_bytes = 0;
+    end_call(h->fwd, t);
     return TL_OK;
 }
 
@@ -452,19 +521,18 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const Shape& s = h->s;
     const size_t tb = tile_bytes(s.K, s.Mi);
-    CallTiming& t = h->bwd;
 
     if (T == 0) {  // dW = X^T dY over an empty sum: zero
-        TL_TRY(h, cudaEventRecord(t.start, cs));
         TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[0], 0));
         TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tb, cs));
         for (int i = 0; i < s.N; ++i) TL_TRY(h, copy_dw_tile(h, i, h->stage[0], cs));
         TL_TRY(h, cudaEventRecord(h->ev_drained[0], cs));
-        TL_TRY(h, cudaEventRecord(t.end, cs));
-        t.valid = false;
         return TL_OK;
     }
 
+    CallSlot* tp = begin_call(h, h->bwd, &st);
+    if (!tp) return st;
+    CallSlot& t = *tp;
     const int nslots = h->d + 1;
     TL_TRY(h, cudaEventRecord(t.start, cs));
     for (int j = 0; j < s.N; ++j) {
@@ -532,11 +600,11 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     for (int g = 0; g < h->nstage; ++g) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[g], 0));
     TL_TRY(h, cudaEventRecord(t.end, cs));
     TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
-    t.valid = true;
     t.depth = h->d;
     t.launches = 2 * s.N;
     t.h2d_bytes = int64_t(s.N) * int64_t(tb);
     t.d2h_bytes = int64_t(s.N) * int64_t(tb);
+    end_call(h->bwd, t);
     return TL_OK;
 }
 
@@ -554,10 +622,11 @@ tl_status tiled_linear_destroy(tl_handle* h) {
                     cudaEventDestroy(e);
                 }
             }
-        if (h->fwd.end) cudaEventSynchronize(h->fwd.end);
-        if (h->bwd.end) cudaEventSynchronize(h->bwd.end);
-        destroy_events(h->fwd);
-        destroy_events(h->bwd);
+        for (Phase* p : {&h->fwd, &h->bwd})
+            for (auto& c : p->ring)
+                if (c.end) cudaEventSynchronize(c.end);
+        destroy_phase(h->fwd);
+        destroy_phase(h->bwd);
         if (h->h2d) cudaStreamDestroy(h->h2d);
         if (h->d2h) cudaStreamDestroy(h->d2h);
         if (h->err_mirror) cudaFreeHost(h->err_mirror);
@@ -579,43 +648,62 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
     DeviceGuard guard(h->device);
     out->n_tiles = h->s.N;
     out->depth = h->d;
-    const int n = h->s.N;
-    if (h->fwd.valid) {
-        TL_TRY(h, cudaEventSynchronize(h->fwd.end));
-        CallTiming& t = h->fwd;
+    tl_status st = harvest_all(h, h->fwd);
+    if (st == TL_OK) st = harvest_all(h, h->bwd);
+    if (st != TL_OK) return st;
+    if (h->fwd.last >= 0) {
+        const CallSlot& c = h->fwd.ring[h->fwd.last];
         out->fwd_valid = 1;
-        out->fwd_total_ms = span_ms(t.start, t.end);
-        for (int i = 0; i < n; ++i) {
-            out->fwd_gemm_ms += span_ms(t.ev[0][i], t.ev[1][i]);
-            out->fwd_h2d_ms += span_ms(t.ev[4][i], t.ev[5][i]);
-        }
-        out->fwd_wait_ms = out->fwd_total_ms - out->fwd_gemm_ms;
-        out->fwd_h2d_bytes = t.h2d_bytes;
-        out->fwd_launches = t.launches;
-        out->depth = t.depth;
+        out->fwd_total_ms = c.total;
+        out->fwd_gemm_ms = c.gemm1;
+        out->fwd_h2d_ms = c.h2d;
+        out->fwd_wait_ms = c.total - c.gemm1;
+        out->fwd_h2d_bytes = c.h2d_bytes;
+        out->fwd_launches = c.launches;
+        out->depth = c.depth;
     }
-    if (h->bwd.valid) {
-        TL_TRY(h, cudaEventSynchronize(h->bwd.end));
-        CallTiming& t = h->bwd;
+    if (h->bwd.last >= 0) {
+        const CallSlot& c = h->bwd.ring[h->bwd.last];
         out->bwd_valid = 1;
-        out->bwd_total_ms = span_ms(t.start, t.end);
-        for (int j = 0; j < n; ++j) {
-            out->bwd_dw_gemm_ms += span_ms(t.ev[0][j], t.ev[1][j]);
-            out->bwd_dx_gemm_ms += span_ms(t.ev[2][j], t.ev[3][j]);
-            out->bwd_h2d_ms += span_ms(t.ev[4][j], t.ev[5][j]);
-            out->bwd_d2h_ms += span_ms(t.ev[6][j], t.ev[7][j]);
-        }
-        out->bwd_wait_ms = out->bwd_total_ms - out->bwd_dw_gemm_ms - out->bwd_dx_gemm_ms;
-        out->bwd_h2d_bytes = t.h2d_bytes;
-        out->bwd_d2h_bytes = t.d2h_bytes;
-        out->bwd_launches = t.launches;
+        out->bwd_total_ms = c.total;
+        out->bwd_dw_gemm_ms = c.gemm1;
+        out->bwd_dx_gemm_ms = c.gemm2;
+        out->bwd_h2d_ms = c.h2d;
+        out->bwd_d2h_ms = c.d2h;
+        out->bwd_wait_ms = c.total - c.gemm1 - c.gemm2;
+        out->bwd_h2d_bytes = c.h2d_bytes;
+        out->bwd_d2h_bytes = c.d2h_bytes;
+        out->bwd_launches = c.launches;
     }
+    out->fwd_calls = h->fwd.sum_calls;
+    out->sum_fwd_total_ms = h->fwd.sum_total;
+    out->sum_fwd_gemm_ms = h->fwd.sum_gemm1;
+    out->sum_fwd_h2d_ms = h->fwd.sum_h2d;
+    out->bwd_calls = h->bwd.sum_calls;
+    out->sum_bwd_total_ms = h->bwd.sum_total;
+    out->sum_bwd_dw_gemm_ms = h->bwd.sum_gemm1;
+    out->sum_bwd_dx_gemm_ms = h->bwd.sum_gemm2;
+    out->sum_bwd_h2d_ms = h->bwd.sum_h2d;
+    out->sum_bwd_d2h_ms = h->bwd.sum_d2h;
     int32_t word = 0;
     TL_TRY(h, cudaMemcpy(&word, h->err_dev, sizeof(word), cudaMemcpyDeviceToHost));
     if (word != 0)
         return fail(h, TL_ERR_TIMEOUT,
                     "a kernel's bounded wait timed out (error bits " + std::to_string(word) + ")");
     return h->sticky;
+}
+
+tl_status tiled_linear_reset_stats(tl_handle* h) {
+    if (!h) return TL_ERR_INVALID;
+    DeviceGuard guard(h->device);
+    tl_status st = harvest_all(h, h->fwd);
+    if (st == TL_OK) st = harvest_all(h, h->bwd);
+    if (st != TL_OK) return st;
+    for (Phase* p : {&h->fwd, &h->bwd}) {
+        p->sum_calls = 0;
+        p->sum_total = p->sum_gemm1 = p->sum_gemm2 = p->sum_h2d = p->sum_d2h = 0;
+    }
+    return TL_OK;
 }
 
 // ---- resident GEMMs --------------------------------------------------------

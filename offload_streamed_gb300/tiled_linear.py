@@ -38,6 +38,11 @@ class tl_stats(ctypes.Structure):
         ("fwd_wait_ms", ctypes.c_float), ("bwd_wait_ms", ctypes.c_float),
         ("fwd_h2d_bytes", ctypes.c_int64), ("bwd_h2d_bytes", ctypes.c_int64), ("bwd_d2h_bytes", ctypes.c_int64),
         ("fwd_launches", ctypes.c_int32), ("bwd_launches", ctypes.c_int32),
+        ("fwd_calls", ctypes.c_int64), ("bwd_calls", ctypes.c_int64),
+        ("sum_fwd_total_ms", ctypes.c_double), ("sum_fwd_gemm_ms", ctypes.c_double),
+        ("sum_fwd_h2d_ms", ctypes.c_double), ("sum_bwd_total_ms", ctypes.c_double),
+        ("sum_bwd_dw_gemm_ms", ctypes.c_double), ("sum_bwd_dx_gemm_ms", ctypes.c_double),
+        ("sum_bwd_h2d_ms", ctypes.c_double), ("sum_bwd_d2h_ms", ctypes.c_double),
     ]
 
     def as_dict(self) -> dict:
@@ -81,6 +86,8 @@ def load():
         L.tiled_linear_last_error.restype = ctypes.c_char_p
         L.tiled_linear_get_stats.argtypes = [vp, vp]
         L.tiled_linear_get_stats.restype = st
+        L.tiled_linear_reset_stats.argtypes = [vp]
+        L.tiled_linear_reset_stats.restype = st
         L.tiled_linear_gemm_forward.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp]
         L.tiled_linear_gemm_forward.restype = st
         L.tiled_linear_gemm_dw.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp]
@@ -145,6 +152,10 @@ def tiled_linear_get_stats(h: int) -> dict:
     s = tl_stats()
     _check(load().tiled_linear_get_stats(h, ctypes.byref(s)), "tiled_linear_get_stats", h)
     return s.as_dict()
+
+
+def tiled_linear_reset_stats(h: int) -> None:
+    _check(load().tiled_linear_reset_stats(h), "tiled_linear_reset_stats", h)
 
 
 def tiled_linear_gemm_forward(T, K, n, x, ldx, w, ldw, y, ldy, err, stream) -> None:
@@ -259,6 +270,9 @@ class TiledLinear:
 
     def stats(self) -> dict:
         return tiled_linear_get_stats(self.handle)
+
+    def reset_stats(self) -> None:
+        tiled_linear_reset_stats(self.handle)
 
     def close(self) -> int:
         st = TL_OK
