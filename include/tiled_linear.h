@@ -178,6 +178,36 @@ tl_status tiled_linear_gemm_dx(int64_t T, int64_t K, int64_t n,
                                float *dx_dev, int64_t lddx, int32_t accumulate,
                                int32_t *err_dev, void *stream);
 
+/* --- forward without any device allocation --------------------------------
+ * The pages describe no counterpart to this entry point.  It exists for
+ * callers that cannot allocate device memory at all and so cannot supply the
+ * workspace tiled_linear_create needs: for example a plug-in running inside a
+ * framework whose allocator owns all of the GPU's memory, or a service that
+ * forbids new allocations once it has started.
+ *
+ * Computes the same Y as tiled_linear_forward for W stored tile-major
+ * [N][K][Mi] in pinned host memory, with the same kernel and tile order, so Y
+ * is identical.  Its scratch (one weight-tile slot and the kernels' timeout
+ * word) is a 32 MiB static device array inside this library, which every GPU
+ * that loads the library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *  - Limit: one tile, K*(M/N)*2 bytes, must fit in 32 MiB - 256 bytes; a
+ *    larger tile returns TL_ERR_WORKSPACE (split W into more tiles).
+ *  - Every copy and GEMM is ordered on `stream`, so copies do not overlap the
+ *    GEMMs.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls share the array, which keeps the last call's contents (the
+ *    timeout word is cleared at the start of each call).  Calls whose work
+ *    overlaps on the GPU (other streams, other host threads) race on it:
+ *    order them.
+ *  - status_host: optional (NULL or pinned host int32); receives the kernels'
+ *    timeout word once `stream` completes (0 = no timeout).
+ * Errors: TL_ERR_INVALID, TL_ERR_NOT_PINNED, TL_ERR_WORKSPACE, TL_ERR_CUDA. */
+tl_status tiled_linear_forward_static(int64_t T, int64_t K, int64_t M, int32_t N,
+                                      const void *w_host, const void *x_dev, void *y_dev,
+                                      int32_t *status_host, void *stream);
+
 /* --- pinned host memory helpers ------------------------------------------ */
 /* Page-locked host allocation (cudaHostAlloc, portable); *out = NULL on
  * failure.  Free with tiled_linear_host_free. */

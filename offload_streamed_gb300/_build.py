@@ -1,7 +1,7 @@
 """Build the CUDA library in-tree: ``offload_streamed_gb300/_lib/libtiled_linear.so``.
 
-Two translation units (the GEMM kernels and the engine / C ABI) are compiled
-in parallel by nvcc for sm_103a only, then linked against the shared CUDA
+The translation units (GEMM kernels, engine / C ABI, allocation-free
+forward) are compiled in parallel by nvcc for sm_103a only, then linked against the shared CUDA
 runtime (the same ``libcudart.so.13`` PyTorch loads, so streams created by
 either side are one runtime's streams).  The build is skipped when the shared
 library is newer than every source and header.
@@ -24,7 +24,7 @@ LIB = os.path.join(LIBDIR, "libtiled_linear.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I", INCLUDE, "-I", CSRC]
-UNITS = ["tl_gemm.cu", "tl_engine.cu"]
+UNITS = ["tl_gemm.cu", "tl_engine.cu", "tl_static.cu"]
 
 
 def nvcc() -> str:

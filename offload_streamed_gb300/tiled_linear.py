@@ -94,6 +94,8 @@ def load():
         L.tiled_linear_gemm_dw.restype = st
         L.tiled_linear_gemm_dx.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp, vp]
         L.tiled_linear_gemm_dx.restype = st
+        L.tiled_linear_forward_static.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp]
+        L.tiled_linear_forward_static.restype = st
         L.tiled_linear_host_alloc.argtypes = [sz, ctypes.POINTER(vp)]
         L.tiled_linear_host_alloc.restype = st
         L.tiled_linear_host_free.argtypes = [vp]
@@ -171,6 +173,14 @@ def tiled_linear_gemm_dw(T, K, n, x, ldx, dy, lddy, dw, lddw, err, stream) -> No
 def tiled_linear_gemm_dx(T, K, n, dy, lddy, w, ldw, dx, lddx, accumulate, err, stream) -> None:
     _check(load().tiled_linear_gemm_dx(T, K, n, dy, lddy, w, ldw, dx, lddx, int(accumulate), err, stream),
            "tiled_linear_gemm_dx")
+
+
+def tiled_linear_forward_static(T, K, M, N, w_host, x_dev, y_dev, status_host, stream) -> None:
+    """Forward with no device allocation (scratch in a static device array);
+    see the header for its limit and ordering rules."""
+    st = load().tiled_linear_forward_static(T, K, M, N, w_host, x_dev, y_dev, status_host, stream)
+    if st != TL_OK:
+        raise TiledLinearError(st, "tiled_linear_forward_static")
 
 
 def tiled_linear_host_alloc(nbytes: int) -> int:
