@@ -27,31 +27,43 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <climits>
+#include <cstdlib>
 #include <mutex>
 
 namespace tl {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kUmmaK = 16;
-constexpr uint32_t kStageA = kBlockM * kBlockK * 2;  // 16 KiB
-constexpr uint32_t kStageB = kBlockN * kBlockK * 2;  // 32 KiB
-constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr uint32_t kStageA = kBlockM * kBlockK * 2;  // 128 rows of A per CTA: 16 KiB
 constexpr uint32_t kMnChunk = 64 * kBlockK * 2;      // 64 MN elements x 64 K rows = 8 KiB
 constexpr uint32_t kTmemCols = 2 * kBlockN;          // two fp32 accumulators of 256 columns
 constexpr int kThreads = 256;
 constexpr int kFirstEpilogueWarp = 4;
-constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 256 + 1024;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr int kGroupM = 16;
 
 static_assert(kBlockK * 2 == 128, "one K-block row must be one 128-byte swizzle row");
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// Tile geometry.  Single CTA: 128 x 256 output tile, B = 256 rows of N per
+// stage.  CTA pair (cta_group::2): 256 x 256 output tile; each CTA loads its
+// own 128 rows of A and its own 128 rows (N) of B, and the pair's MMA reads
+// both CTAs' shared memory.
+template <bool PAIR>
+struct Geo {
+    static constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;
+    static constexpr int kBRows = PAIR ? kBlockN / 2 : kBlockN;
+    static constexpr uint32_t kStageB = uint32_t(kBRows) * kBlockK * 2;
+    static constexpr uint32_t kStageBytes = kStageA + kStageB;
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 256 + 1024;
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
 
 struct KParams {
     int32_t m_dim, n_dim, k_dim;
     int32_t num_m, num_n, num_k, num_tiles;
+    int32_t raster, group;  // raster 0: groups of `group` m-blocks (m fastest); 1: groups of n-blocks
     void* d;
     int64_t ldd;
     int32_t accumulate;
@@ -93,14 +105,21 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t
     return __all_sync(0xffffffffu, mine) != 0;
 }
 
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
-    const int group_tiles = kGroupM * num_n;
+// Output tile order: groups of `group` blocks along one dimension, walking
+// the other dimension inside the group, so that the group's blocks of one
+// operand stay in L2 while the other operand streams past once per group.
+__device__ __forceinline__ void tile_coords(int tile, const KParams& p, int& mb, int& nb) {
+    const int outer = p.raster == 0 ? p.num_m : p.num_n;
+    const int inner = p.raster == 0 ? p.num_n : p.num_m;
+    const int group_tiles = p.group * inner;
     const int g = tile / group_tiles;
-    const int first_m = g * kGroupM;
-    const int gm = min(kGroupM, num_m - first_m);
+    const int first = g * p.group;
+    const int width = min(p.group, outer - first);
     const int local = tile - g * group_tiles;
-    mb = first_m + local % gm;
-    nb = local / gm;
+    const int a = first + local % width;
+    const int b = local / width;
+    mb = p.raster == 0 ? a : b;
+    nb = p.raster == 0 ? b : a;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -158,114 +177,129 @@ __device__ __forceinline__ void store_chunk(const KParams& p, int64_t row, int c
     }
 }
 
-template <bool A_MN, bool B_MN, bool OUT_F32>
+template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const KParams p) {
+    using G = Geo<PAIR>;
+    constexpr int S = G::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * G::kStageBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int first_tile = PAIR ? int(cluster_id_x()) : int(blockIdx.x);
+    const int tile_step = PAIR ? int(cluster_count_x()) : int(gridDim.x);
+    const bool leader = (rank == 0);
     const uint32_t bar0 = smem_addr(bars);
     const uint32_t smem0 = smem_addr(smem);
-    // barrier addresses: full[s], empty[s], tmem_full[a], tmem_empty[a], drain
+    // barriers: full[s], empty[s], tmem_full[a], tmem_empty[a], drain.  With
+    // a CTA pair, full[] and tmem_empty[] are used in the first CTA only.
     auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (kStages + s); };
-    auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + a); };
-    auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + 2 + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (S + s); };
+    auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * S + a); };
+    auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+            mbar_init(tempty_bar(a), PAIR ? 8 : 4);  // one arrival per epilogue warp of the tile
         }
         mbar_init(drain_bar, 1);
         mbar_init_fence();
     }
     if (warp == 2) {
-        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<PAIR>(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish<PAIR>();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer ----------------
+            // ---------------- TMA producer (each CTA loads its own halves) ----------------
             tma_prefetch_map(&map_a);
             tma_prefetch_map(&map_b);
             uint32_t fills = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step) {
                 int mb, nb;
-                tile_coords(tile, p.num_m, p.num_n, mb, nb);
-                const int m0 = mb * kBlockM, n0 = nb * kBlockN;
+                tile_coords(tile, p, mb, nb);
+                const int m0 = mb * G::kTileM + int(rank) * kBlockM;
+                const int n0 = nb * kBlockN + int(rank) * (PAIR ? G::kBRows : 0);
                 for (int kb = 0; kb < p.num_k; ++kb, ++fills) {
-                    const uint32_t s = fills % kStages;
-                    const uint32_t ph = (fills / kStages) & 1u;
+                    const uint32_t s = fills % S;
+                    const uint32_t ph = (fills / S) & 1u;
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, p.err, kErrProducerWait)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = smem0 + s * kStageBytes;
+                    const uint32_t sa = smem0 + s * G::kStageBytes;
                     const uint32_t sb = sa + kStageA;
                     const int k0 = kb * kBlockK;
-                    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+                    if (leader) mbar_arrive_expect_tx(full_bar(s), (PAIR ? 2u : 1u) * G::kStageBytes);
+                    const uint32_t fb = PAIR ? map_to_rank(full_bar(s), 0) : full_bar(s);
+                    auto load = [&](uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y) {
+                        if constexpr (PAIR) tma_load_2d_pair(dst, m, fb, x, y);
+                        else tma_load_2d(dst, m, fb, x, y);
+                    };
                     if (A_MN) {
-                        tma_load_2d(sa, &map_a, full_bar(s), m0, k0);
-                        tma_load_2d(sa + kMnChunk, &map_a, full_bar(s), m0 + 64, k0);
+                        load(sa, &map_a, m0, k0);
+                        load(sa + kMnChunk, &map_a, m0 + 64, k0);
                     } else {
-                        tma_load_2d(sa, &map_a, full_bar(s), k0, m0);
+                        load(sa, &map_a, k0, m0);
                     }
                     if (B_MN) {
 #pragma unroll
-                        for (int c = 0; c < kBlockN / 64; ++c)
-                            tma_load_2d(sb + c * kMnChunk, &map_b, full_bar(s), n0 + 64 * c, k0);
+                        for (int c = 0; c < G::kBRows / 64; ++c) load(sb + c * kMnChunk, &map_b, n0 + 64 * c, k0);
                     } else {
-                        tma_load_2d(sb, &map_b, full_bar(s), k0, n0);
+                        load(sb, &map_b, k0, n0);
                     }
                 }
             }
-            // Our own loads must land before the CTA may exit.
-            const uint32_t outstanding = fills < uint32_t(kStages) ? fills : uint32_t(kStages);
-            for (uint32_t j = 0; j < outstanding; ++j) {
-                const uint32_t f = fills - 1 - j;
-                wait_bounded(full_bar(f % kStages), (f / kStages) & 1u, p.err, kErrDrainWait, false);
+            // Loads must land before the CTA may exit.  The first CTA's full[]
+            // barriers count both CTAs' bytes, so its drain covers the pair.
+            if (leader) {
+                const uint32_t outstanding = fills < uint32_t(S) ? fills : uint32_t(S);
+                for (uint32_t j = 0; j < outstanding; ++j) {
+                    const uint32_t f = fills - 1 - j;
+                    wait_bounded(full_bar(f % S), (f / S) & 1u, p.err, kErrDrainWait, false);
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, A_MN, B_MN);
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (first CTA of the pair) ----------------
+            constexpr uint32_t idesc = idesc_bf16_f32(G::kTileM, kBlockN, A_MN, B_MN);
             uint32_t fills = 0;
             bool ok = true;
             int it = 0;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+            for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step, ++it) {
                 const uint32_t acc = it & 1;
                 const uint32_t acc_ph = (it >> 1) & 1;
                 if (!wait_bounded(tempty_bar(acc), acc_ph ^ 1u, p.err, kErrMmaWaitTmem)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBlockN;
                 for (int kb = 0; kb < p.num_k; ++kb, ++fills) {
-                    const uint32_t s = fills % kStages;
-                    const uint32_t ph = (fills / kStages) & 1u;
+                    const uint32_t s = fills % S;
+                    const uint32_t ph = (fills / S) & 1u;
                     if (!wait_bounded(full_bar(s), ph, p.err, kErrMmaWaitFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem0 + s * kStageBytes;
+                    const uint32_t sa = smem0 + s * G::kStageBytes;
                     const uint32_t sb = sa + kStageA;
 #pragma unroll
                     for (int j = 0; j < kBlockK / kUmmaK; ++j) {
@@ -273,28 +307,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  : smem_desc_sw128(sa + j * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc_sw128(sb + j * 2048, kMnChunk, 1024)
                                                  : smem_desc_sw128(sb + j * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                        if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                        else umma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                     }
-                    umma_commit(empty_bar(s));
+                    if constexpr (PAIR) umma_commit_pair(empty_bar(s), 0x3);
+                    else umma_commit(empty_bar(s));
                 }
-                if (ok) umma_commit(tfull_bar(acc));
+                if (ok) {
+                    if constexpr (PAIR) umma_commit_pair(tfull_bar(acc), 0x3);
+                    else umma_commit(tfull_bar(acc));
+                }
             }
-            // Our own MMAs must complete before TMEM is freed.
-            umma_commit(drain_bar);
+            // The MMAs must complete before TMEM is freed (in both CTAs).
+            if constexpr (PAIR) umma_commit_pair(drain_bar, 0x3);
+            else umma_commit(drain_bar);
             wait_bounded(drain_bar, 0, p.err, kErrDrainWait, false);
         }
     } else if (warp >= kFirstEpilogueWarp) {
-        // ---------------- epilogue ----------------
+        // ---------------- epilogue (each CTA stores its own 128 rows) ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         int it = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+        for (int tile = first_tile; tile < p.num_tiles; tile += tile_step, ++it) {
             const uint32_t acc = it & 1;
             const uint32_t acc_ph = (it >> 1) & 1;
             if (!warp_wait(tfull_bar(acc), acc_ph, p.err, kErrEpilogueWait, lane)) break;
             tc_fence_after();
             int mb, nb;
-            tile_coords(tile, p.num_m, p.num_n, mb, nb);
-            const int64_t row = int64_t(mb) * kBlockM + q * 32 + lane;
+            tile_coords(tile, p, mb, nb);
+            const int64_t row = int64_t(mb) * G::kTileM + int(rank) * kBlockM + q * 32 + lane;
             const int n0 = nb * kBlockN;
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * kBlockN;
             for (int c = 0; c < kBlockN; c += 32) {
@@ -306,15 +346,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) {
+                if (PAIR && !leader) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+                else mbar_arrive(tempty_bar(acc));
+            }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync(); else __syncthreads();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        // The second CTA of a pair has not watched the MMAs: wait for the
+        // drain commit that the first CTA multicast to it.
+        if (PAIR && !leader) wait_bounded(drain_bar, 0, p.err, kErrDrainWait, false);
+        tmem_dealloc<PAIR>(tmem_base, kTmemCols);
     }
 }
 
@@ -359,15 +405,63 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
     return true;
 }
 
-template <bool A_MN, bool B_MN, bool OUT_F32>
+template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp, int grid,
                        cudaStream_t stream) {
-    auto kern = gemm_kernel<A_MN, B_MN, OUT_F32>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
+    auto kern = gemm_kernel<A_MN, B_MN, OUT_F32, PAIR>;
+    constexpr size_t smem = Geo<PAIR>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, kp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, kp);
+}
+
+template <bool PAIR>
+cudaError_t dispatch(const GemmDesc& g, const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
+                     int grid, cudaStream_t stream) {
+    if (!g.a_mn_major && g.b_mn_major) return launch_one<false, true, false, PAIR>(ma, mb, kp, grid, stream);
+    if (g.a_mn_major && g.b_mn_major) return launch_one<true, true, false, PAIR>(ma, mb, kp, grid, stream);
+    return launch_one<false, false, true, PAIR>(ma, mb, kp, grid, stream);
+}
+
+// Choose the tile order that moves the fewest operand bytes from DRAM: keep
+// a group of one operand's blocks (at most kL2Budget bytes) resident in L2
+// and stream the other operand once per group.
+void choose_raster(const GemmDesc& g, int tile_m, KParams& kp) {
+    constexpr double kL2Budget = 64.0 * 1024 * 1024;
+    const double a_blk = double(tile_m) * double(g.k_dim) * 2;
+    const double b_blk = double(kBlockN) * double(g.k_dim) * 2;
+    const double a_tot = a_blk * kp.num_m, b_tot = b_blk * kp.num_n;
+    const int gm = std::max(1, std::min(kp.num_m, int(kL2Budget / a_blk)));
+    const int gn = std::max(1, std::min(kp.num_n, int(kL2Budget / b_blk)));
+    const double t0 = a_tot + b_tot * double((kp.num_m + gm - 1) / gm);
+    const double t1 = b_tot + a_tot * double((kp.num_n + gn - 1) / gn);
+    if (t1 < t0) {
+        kp.raster = 1;
+        kp.group = gn;
+    } else {
+        kp.raster = 0;
+        kp.group = gm;
+    }
+}
+
+bool use_pair() {
+    static const bool pair = [] {
+        const char* e = std::getenv("TILED_LINEAR_CTA_PAIR");
+        return !(e && e[0] == '0');
+    }();
+    return pair;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -389,7 +483,7 @@ std::string gemm_check(const GemmDesc& g) {
     if (g.n_dim > g.ldd) return "D leading dimension too small";
     if (g.lda * 2 >= (int64_t(1) << 40) || g.ldb * 2 >= (int64_t(1) << 40))
         return "leading dimension too large";
-    const int64_t tiles = ((g.m_dim + kBlockM - 1) / kBlockM) * ((g.n_dim + kBlockN - 1) / kBlockN);
+    const int64_t tiles = ((g.m_dim + kBlockM - 1) / kBlockM) * ((g.n_dim + kBlockN - 1) / kBlockN);  // 1-CTA tiles bound pair tiles
     if (tiles > INT32_MAX) return "too many output tiles";
     const bool fwd = !g.a_mn_major && g.b_mn_major && g.out == OutKind::BF16;
     const bool dw = g.a_mn_major && g.b_mn_major && g.out == OutKind::BF16;
@@ -405,35 +499,36 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
         if (why) *why = bad;
         return cudaErrorInvalidValue;
     }
+    const bool pair = use_pair() && num_sms >= 2;
+    const int tile_m = pair ? 2 * kBlockM : kBlockM;
+    const uint32_t b_rows = pair ? kBlockN / 2 : kBlockN;
     CUtensorMap ma, mb;
     const bool ok_a = g.a_mn_major ? make_map(&ma, g.a, g.m_dim, g.k_dim, g.lda, 64, why)
                                    : make_map(&ma, g.a, g.k_dim, g.m_dim, g.lda, kBlockM, why);
     if (!ok_a) return cudaErrorInvalidValue;
     const bool ok_b = g.b_mn_major ? make_map(&mb, g.b, g.n_dim, g.k_dim, g.ldb, 64, why)
-                                   : make_map(&mb, g.b, g.k_dim, g.n_dim, g.ldb, kBlockN, why);
+                                   : make_map(&mb, g.b, g.k_dim, g.n_dim, g.ldb, b_rows, why);
     if (!ok_b) return cudaErrorInvalidValue;
 
     KParams kp{};
     kp.m_dim = int32_t(g.m_dim);
     kp.n_dim = int32_t(g.n_dim);
     kp.k_dim = int32_t(g.k_dim);
-    kp.num_m = int32_t((g.m_dim + kBlockM - 1) / kBlockM);
+    kp.num_m = int32_t((g.m_dim + tile_m - 1) / tile_m);
     kp.num_n = int32_t((g.n_dim + kBlockN - 1) / kBlockN);
     kp.num_k = int32_t((g.k_dim + kBlockK - 1) / kBlockK);
     kp.num_tiles = kp.num_m * kp.num_n;
+    choose_raster(g, tile_m, kp);
     kp.d = g.d;
     kp.ldd = g.ldd;
     kp.accumulate = g.accumulate ? 1 : 0;
     kp.err = g.err;
-    const int grid = kp.num_tiles < num_sms ? kp.num_tiles : num_sms;
+    const int slots = pair ? num_sms / 2 : num_sms;
+    const int units = kp.num_tiles < slots ? kp.num_tiles : slots;
+    const int grid = pair ? 2 * units : units;
 
-    cudaError_t e;
-    if (!g.a_mn_major && g.b_mn_major)
-        e = launch_one<false, true, false>(ma, mb, kp, grid, stream);
-    else if (g.a_mn_major && g.b_mn_major)
-        e = launch_one<true, true, false>(ma, mb, kp, grid, stream);
-    else
-        e = launch_one<false, false, true>(ma, mb, kp, grid, stream);
+    const cudaError_t e = pair ? dispatch<true>(g, ma, mb, kp, grid, stream)
+                               : dispatch<false>(g, ma, mb, kp, grid, stream);
     if (e != cudaSuccess && why) *why = std::string("kernel launch: ") + cudaGetErrorString(e);
     return e;
 }
