@@ -231,6 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- TMA producer (each CTA loads its own halves) ----------------
             tma_prefetch_map(&map_a);
             tma_prefetch_map(&map_b);
+            // the tile order keeps a group of A blocks (raster 0) or of B
+            // blocks (raster 1) in L2; the other operand streams through
+            const uint64_t pol_a = p.raster == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
+            const uint64_t pol_b = p.raster == 0 ? l2_policy_evict_first() : l2_policy_evict_last();
             uint32_t fills = 0;
             bool ok = true;
             for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step) {
@@ -250,21 +254,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int k0 = kb * kBlockK;
                     if (leader) mbar_arrive_expect_tx(full_bar(s), (PAIR ? 2u : 1u) * G::kStageBytes);
                     const uint32_t fb = PAIR ? map_to_rank(full_bar(s), 0) : full_bar(s);
-                    auto load = [&](uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y) {
-                        if constexpr (PAIR) tma_load_2d_pair(dst, m, fb, x, y);
-                        else tma_load_2d(dst, m, fb, x, y);
+                    auto load = [&](uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, uint64_t pol) {
+                        if constexpr (PAIR) tma_load_2d_pair_hint(dst, m, fb, x, y, pol);
+                        else tma_load_2d_hint(dst, m, fb, x, y, pol);
                     };
                     if (A_MN) {
-                        load(sa, &map_a, m0, k0);
-                        load(sa + kMnChunk, &map_a, m0 + 64, k0);
+                        load(sa, &map_a, m0, k0, pol_a);
+                        load(sa + kMnChunk, &map_a, m0 + 64, k0, pol_a);
                     } else {
-                        load(sa, &map_a, k0, m0);
+                        load(sa, &map_a, k0, m0, pol_a);
                     }
                     if (B_MN) {
 #pragma unroll
-                        for (int c = 0; c < G::kBRows / 64; ++c) load(sb + c * kMnChunk, &map_b, n0 + 64 * c, k0);
+                        for (int c = 0; c < G::kBRows / 64; ++c)
+                            load(sb + c * kMnChunk, &map_b, n0 + 64 * c, k0, pol_b);
                     } else {
-                        load(sb, &map_b, k0, n0);
+                        load(sb, &map_b, k0, n0, pol_b);
                     }
                 }
             }
