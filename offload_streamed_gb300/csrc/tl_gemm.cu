@@ -42,6 +42,10 @@ constexpr uint32_t kTmemCols = 2 * kBlockN;          // two fp32 accumulators of
 constexpr int kThreads = 256;
 constexpr int kFirstEpilogueWarp = 4;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+// Epilogue staging: each of the 4 epilogue warps owns a few boxes of 32
+// output rows x 128 bytes (32 fp32 or 64 bf16 columns) for its TMA traffic.
+constexpr uint32_t kEpiBuf = 32 * 128;
+constexpr uint32_t kBarBytes = 512;
 
 static_assert(kBlockK * 2 == 128, "one K-block row must be one 128-byte swizzle row");
 
@@ -49,14 +53,20 @@ static_assert(kBlockK * 2 == 128, "one K-block row must be one 128-byte swizzle 
 // stage.  CTA pair (cta_group::2): 256 x 256 output tile; each CTA loads its
 // own 128 rows of A and its own 128 rows (N) of B, and the pair's MMA reads
 // both CTAs' shared memory.
-template <bool PAIR>
+// bf16 outputs leave through TMA stores of 128B-swizzled staging boxes (2
+// per epilogue warp); fp32 outputs (dX, possibly accumulated) are written by
+// the epilogue threads directly, which keeps shared-memory bandwidth for the
+// tensor cores' operand reads.
+template <bool PAIR, bool OUT_F32>
 struct Geo {
     static constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;
     static constexpr int kBRows = PAIR ? kBlockN / 2 : kBlockN;
     static constexpr uint32_t kStageB = uint32_t(kBRows) * kBlockK * 2;
     static constexpr uint32_t kStageBytes = kStageA + kStageB;
+    static constexpr int kEpiBoxes = OUT_F32 ? 0 : 2;
+    static constexpr uint32_t kEpiBytes = 4u * kEpiBoxes * kEpiBuf;
     static constexpr int kStages = PAIR ? 6 : 4;
-    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 256 + 1024;
+    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + kEpiBytes + kBarBytes + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -127,66 +137,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <bool OUT_F32>
-__device__ __forceinline__ void store_chunk(const KParams& p, int64_t row, int col,
-                                            const uint32_t (&v)[32]) {
-    const int rem = p.n_dim - col;
-    if constexpr (OUT_F32) {
-        float* out = static_cast<float*>(p.d) + row * p.ldd + col;
-        if (rem >= 32) {
-            float4* o = reinterpret_cast<float4*>(out);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float4 val = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                         __uint_as_float(v[4 * j + 2]),
-                                         __uint_as_float(v[4 * j + 3]));
-                if (p.accumulate) {
-                    const float4 old = o[j];
-                    val.x = old.x + val.x;
-                    val.y = old.y + val.y;
-                    val.z = old.z + val.z;
-                    val.w = old.w + val.w;
-                }
-                o[j] = val;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (j < rem) {
-                    const float val = __uint_as_float(v[j]);
-                    out[j] = p.accumulate ? out[j] + val : val;
-                }
-            }
-        }
-    } else {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col;
-        if (rem >= 32) {
-            uint4* o = reinterpret_cast<uint4*>(out);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                o[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-                                  pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                                  pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                                  pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (j < rem) out[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
-        }
-    }
-}
-
 template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const KParams p) {
-    using G = Geo<PAIR>;
+                const __grid_constant__ CUtensorMap map_d, const KParams p) {
+    using G = Geo<PAIR, OUT_F32>;
     constexpr int S = G::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * G::kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * G::kStageBytes + G::kEpiBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
 
     const int warp = threadIdx.x >> 5;
@@ -330,24 +290,122 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kFirstEpilogueWarp) {
         // ---------------- epilogue (each CTA stores its own 128 rows) ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // Warp q owns TMEM lanes 32q..32q+31 = output rows row0..row0+31 of
+        // the CTA's half tile; lane l holds row row0 + l.
+        //  bf16: per 64-column chunk, two tcgen05.ld, pack, write the lane's
+        //    128-byte row into a 128B-swizzled staging box; one lane issues a
+        //    TMA store of the 32 x 64 box (double-buffered).
+        //  fp32: per 32-column chunk, tcgen05.ld and a direct 128-byte store of
+        //    the lane's row; when accumulating, the old values of the next
+        //    chunk are loaded while the current one is added and stored.
+        constexpr int kChunk = OUT_F32 ? 32 : 64;
+        const int q = warp & 3;
+        const uint32_t epi0 = smem0 + S * G::kStageBytes + uint32_t(q) * 2u * kEpiBuf;
+        if (!OUT_F32 && lane == 0) tma_prefetch_map(&map_d);
+        uint32_t buf = 0;
         int it = 0;
         for (int tile = first_tile; tile < p.num_tiles; tile += tile_step, ++it) {
             const uint32_t acc = it & 1;
             const uint32_t acc_ph = (it >> 1) & 1;
-            if (!warp_wait(tfull_bar(acc), acc_ph, p.err, kErrEpilogueWait, lane)) break;
-            tc_fence_after();
             int mb, nb;
             tile_coords(tile, p, mb, nb);
-            const int64_t row = int64_t(mb) * G::kTileM + int(rank) * kBlockM + q * 32 + lane;
+            const int row0 = mb * G::kTileM + int(rank) * kBlockM + q * 32;
             const int n0 = nb * kBlockN;
+            int nchunks = 0;
+            if (row0 < p.m_dim)  // warp-uniform
+                while (nchunks * kChunk < kBlockN && n0 + nchunks * kChunk < p.n_dim) ++nchunks;
+            if (!warp_wait(tfull_bar(acc), acc_ph, p.err, kErrEpilogueWait, lane)) break;
+            tc_fence_after();
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * kBlockN;
-            for (int c = 0; c < kBlockN; c += 32) {
-                if (n0 + c >= p.n_dim) break;  // warp-uniform
-                uint32_t v[32];
-                tmem_ld_32cols(t_row + c, v);
-                tmem_ld_wait();
-                if (row < p.m_dim) store_chunk<OUT_F32>(p, row, n0 + c, v);
+            if constexpr (OUT_F32) {
+                const int64_t row = int64_t(row0) + lane;
+                const bool row_ok = row < p.m_dim;
+                float* out_row = static_cast<float*>(p.d) + row * p.ldd + n0;
+                const bool rmw = p.accumulate != 0;
+                float4 old[8];
+                auto load_old = [&](int c, float4 (&dst)[8]) {
+                    const float* src = out_row + c * kChunk;
+                    const int rem = p.n_dim - (n0 + c * kChunk);
+                    if (row_ok && rem >= 32) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) dst[j] = reinterpret_cast<const float4*>(src)[j];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            dst[j].x = (row_ok && 4 * j + 0 < rem) ? src[4 * j + 0] : 0.f;
+                            dst[j].y = (row_ok && 4 * j + 1 < rem) ? src[4 * j + 1] : 0.f;
+                            dst[j].z = (row_ok && 4 * j + 2 < rem) ? src[4 * j + 2] : 0.f;
+                            dst[j].w = (row_ok && 4 * j + 3 < rem) ? src[4 * j + 3] : 0.f;
+                        }
+                    }
+                };
+                if (rmw && nchunks > 0) load_old(0, old);
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t w[32];
+                    tmem_ld_32cols(t_row + c * kChunk, w);
+                    float4 nxt[8];
+                    if (rmw && c + 1 < nchunks) load_old(c + 1, nxt);
+                    tmem_ld_wait();
+                    float4 val[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        val[j] = make_float4(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]),
+                                             __uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]));
+                        if (rmw) {
+                            val[j].x = old[j].x + val[j].x;
+                            val[j].y = old[j].y + val[j].y;
+                            val[j].z = old[j].z + val[j].z;
+                            val[j].w = old[j].w + val[j].w;
+                        }
+                    }
+                    float* dst = out_row + c * kChunk;
+                    const int rem = p.n_dim - (n0 + c * kChunk);
+                    if (row_ok && rem >= 32) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) reinterpret_cast<float4*>(dst)[j] = val[j];
+                    } else if (row_ok) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (4 * j + 0 < rem) dst[4 * j + 0] = val[j].x;
+                            if (4 * j + 1 < rem) dst[4 * j + 1] = val[j].y;
+                            if (4 * j + 2 < rem) dst[4 * j + 2] = val[j].z;
+                            if (4 * j + 3 < rem) dst[4 * j + 3] = val[j].w;
+                        }
+                    }
+                    if (rmw && c + 1 < nchunks) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) old[j] = nxt[j];
+                    }
+                }
+            } else {
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t w[32];  // this lane's 128-byte row of the chunk (64 bf16)
+                    uint32_t v[32];
+                    tmem_ld_32cols(t_row + c * kChunk, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    tmem_ld_32cols(t_row + c * kChunk + 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        w[16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    const uint32_t sbuf = epi0 + buf * kEpiBuf;
+                    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used sbuf has read it
+                    __syncwarp();
+                    const uint32_t row_addr = sbuf + uint32_t(lane) * 128u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(row_addr + ((uint32_t(j) ^ (uint32_t(lane) & 7u)) << 4), w[4 * j],
+                                     w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&map_d, sbuf, n0 + c * kChunk, row0);
+                        bulk_commit_group();
+                    }
+                    buf ^= 1u;
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -356,6 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else mbar_arrive(tempty_bar(acc));
             }
         }
+        if (!OUT_F32 && lane == 0) bulk_wait_group_all();  // stores complete before the CTA exits
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -386,21 +446,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows
-// `ld` elements apart, box of 64 x box_outer, 128-byte swizzle, zero fill
-// outside the tensor.
+// 2-D tensor map: `inner` contiguous elements per row, `outer` rows `ld`
+// elements apart, box of (128 bytes of elements) x box_outer, 128-byte
+// swizzle, zero fill outside the tensor (loads) / clipping (stores).
 bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-              uint32_t box_outer, std::string* why) {
+              uint32_t box_outer, std::string* why, bool f32 = false) {
     auto fn = encode_fn();
     if (!fn) {
         if (why) *why = "cuTensorMapEncodeTiled is unavailable from the driver";
         return false;
     }
+    const uint32_t esize = f32 ? 4 : 2;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {ld * 2};
-    cuuint32_t box[2] = {64, box_outer};
+    cuuint64_t strides[1] = {ld * esize};
+    cuuint32_t box[2] = {128 / esize, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+    CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -411,10 +473,10 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 }
 
 template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
-cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp, int grid,
-                       cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const KParams& kp,
+                       int grid, cudaStream_t stream) {
     auto kern = gemm_kernel<A_MN, B_MN, OUT_F32, PAIR>;
-    constexpr size_t smem = Geo<PAIR>::kSmem;
+    constexpr size_t smem = Geo<PAIR, OUT_F32>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -429,15 +491,15 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const KPara
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ma, mb, kp);
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, md, kp);
 }
 
 template <bool PAIR>
-cudaError_t dispatch(const GemmDesc& g, const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
-                     int grid, cudaStream_t stream) {
-    if (!g.a_mn_major && g.b_mn_major) return launch_one<false, true, false, PAIR>(ma, mb, kp, grid, stream);
-    if (g.a_mn_major && g.b_mn_major) return launch_one<true, true, false, PAIR>(ma, mb, kp, grid, stream);
-    return launch_one<false, false, true, PAIR>(ma, mb, kp, grid, stream);
+cudaError_t dispatch(const GemmDesc& g, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                     const KParams& kp, int grid, cudaStream_t stream) {
+    if (!g.a_mn_major && g.b_mn_major) return launch_one<false, true, false, PAIR>(ma, mb, md, kp, grid, stream);
+    if (g.a_mn_major && g.b_mn_major) return launch_one<true, true, false, PAIR>(ma, mb, md, kp, grid, stream);
+    return launch_one<false, false, true, PAIR>(ma, mb, md, kp, grid, stream);
 }
 
 // Choose the tile order that moves the fewest operand bytes from DRAM: keep
@@ -514,6 +576,8 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     const bool ok_b = g.b_mn_major ? make_map(&mb, g.b, g.n_dim, g.k_dim, g.ldb, 64, why)
                                    : make_map(&mb, g.b, g.k_dim, g.n_dim, g.ldb, b_rows, why);
     if (!ok_b) return cudaErrorInvalidValue;
+    CUtensorMap md;
+    if (!make_map(&md, g.d, g.n_dim, g.m_dim, g.ldd, 32, why, g.out == OutKind::F32)) return cudaErrorInvalidValue;
 
     KParams kp{};
     kp.m_dim = int32_t(g.m_dim);
@@ -532,8 +596,8 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     const int units = kp.num_tiles < slots ? kp.num_tiles : slots;
     const int grid = pair ? 2 * units : units;
 
-    const cudaError_t e = pair ? dispatch<true>(g, ma, mb, kp, grid, stream)
-                               : dispatch<false>(g, ma, mb, kp, grid, stream);
+    const cudaError_t e = pair ? dispatch<true>(g, ma, mb, md, kp, grid, stream)
+                               : dispatch<false>(g, ma, mb, md, kp, grid, stream);
     if (e != cudaSuccess && why) *why = std::string("kernel launch: ") + cudaGetErrorString(e);
     return e;
 }
