@@ -178,6 +178,18 @@ tl_status tiled_linear_gemm_dx(int64_t T, int64_t K, int64_t n,
                                float *dx_dev, int64_t lddx, int32_t accumulate,
                                int32_t *err_dev, void *stream);
 
+/* Self-test of the kernels' failure path.  Launches the forward GEMM kernel
+ * on a 128 x 256 x 64 problem with every operand load withheld and every
+ * bounded wait limited to timeout_ns (0 < timeout_ns <= 10 s): the MMA
+ * thread's wait for its first shared-memory stage runs out, it sets bit 2 in
+ * the int32 at scratch_dev (cleared first), every role stops, the kernel
+ * frees its tensor memory and exits -- nothing faults or hangs and the
+ * context stays usable.  scratch_dev: device memory, 256-byte aligned, at
+ * least 65792 bytes (only the first int32 is written).  Stream-ordered.
+ * Errors: TL_ERR_INVALID, TL_ERR_CUDA. */
+tl_status tiled_linear_selftest_timeout(void *scratch_dev, size_t scratch_bytes, int64_t timeout_ns,
+                                        void *stream);
+
 /* --- forward without any device allocation --------------------------------
  * The pages describe no counterpart to this entry point.  It exists for
  * callers that cannot allocate device memory at all and so cannot supply the

@@ -780,6 +780,37 @@ tl_status tiled_linear_gemm_dx(int64_t T, int64_t K, int64_t n, const void* dy_d
     return raw_launch(g, stream);
 }
 
+tl_status tiled_linear_selftest_timeout(void* scratch_dev, size_t scratch_bytes, int64_t timeout_ns,
+                                        void* stream) {
+    constexpr size_t kNeed = 256 + 128 * 256 * 2;
+    if (!scratch_dev || (reinterpret_cast<uintptr_t>(scratch_dev) & 255u) || scratch_bytes < kNeed ||
+        timeout_ns <= 0 || timeout_ns > int64_t(10000000000))
+        return TL_ERR_INVALID;
+    auto* base = static_cast<uint8_t*>(scratch_dev);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(base, 0, sizeof(int32_t), cs) != cudaSuccess) return TL_ERR_CUDA;
+    // A 128 x 256 x 64 forward GEMM whose operands are never read: the
+    // producer withholds every load, so the MMA thread's first bounded wait
+    // runs out.
+    tl::GemmDesc g;
+    g.m_dim = 128;
+    g.n_dim = 256;
+    g.k_dim = 64;
+    g.a = base + 256;
+    g.lda = 64;
+    g.a_mn_major = false;
+    g.b = base + 256;
+    g.ldb = 256;
+    g.b_mn_major = true;
+    g.d = base + 256;
+    g.ldd = 256;
+    g.out = tl::OutKind::BF16;
+    g.err = reinterpret_cast<int32_t*>(base);
+    g.timeout_ns = uint64_t(timeout_ns);
+    g.withhold_loads = true;
+    return raw_launch(g, stream);
+}
+
 tl_status tiled_linear_host_alloc(size_t bytes, void** out) {
     if (!out) return TL_ERR_INVALID;
     *out = nullptr;

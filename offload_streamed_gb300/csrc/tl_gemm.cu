@@ -41,7 +41,6 @@ constexpr uint32_t kMnChunk = 64 * kBlockK * 2;      // 64 MN elements x 64 K ro
 constexpr uint32_t kTmemCols = 2 * kBlockN;          // two fp32 accumulators of 256 columns
 constexpr int kThreads = 256;
 constexpr int kFirstEpilogueWarp = 4;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 // Epilogue staging: each of the 4 epilogue warps owns a few boxes of 32
 // output rows x 128 bytes (32 fp32 or 64 bf16 columns) for its TMA traffic.
 constexpr uint32_t kEpiBuf = 32 * 128;
@@ -77,17 +76,19 @@ struct KParams {
     void* d;
     int64_t ldd;
     int32_t accumulate;
+    int32_t withhold_loads;
     int32_t* err;
+    uint64_t timeout_ns;
 };
 
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int32_t* err, int32_t code,
-                                       bool stop_on_error) {
+                                       bool stop_on_error, uint64_t timeout_ns) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 255u) == 0) {
             if (stop_on_error && *reinterpret_cast<volatile int32_t*>(err) != 0) return false;
-            if (global_timer_ns() - t0 > kTimeoutNs) {
+            if (global_timer_ns() - t0 > timeout_ns) {
                 atomicOr(err, code);
                 return false;
             }
@@ -95,18 +96,24 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int32_t* e
     }
 }
 
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, int32_t* err,
-                                             int32_t code, bool stop_on_error = true) {
+// The MMA thread's waits use the base limit; the producer's wait for a free
+// stage and the epilogue's wait for an accumulator (both downstream of the
+// MMA thread) use twice that, so when a pipeline stalls the role nearest the
+// stall reports first.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const KParams& p, int32_t code,
+                                             bool stop_on_error = true) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, err, code, stop_on_error);
+    const bool downstream = code == kErrProducerWait || code == kErrEpilogueWait;
+    return wait_slow(bar, parity, p.err, code, stop_on_error, downstream ? 2 * p.timeout_ns : p.timeout_ns);
 }
 
 // Warp-uniform wait: lane 0 waits (bounded); then every lane observes the
 // completed phase itself, which cannot move on before this warp arrives.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t* err, int32_t code,
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const KParams& p, int32_t code,
                                           int lane) {
+    int32_t* err = p.err;
     int ok = 1;
-    if (lane == 0) ok = wait_bounded(bar, parity, err, code) ? 1 : 0;
+    if (lane == 0) ok = wait_bounded(bar, parity, p, code) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) return false;
     int mine = 0;
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_a = p.raster == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
             const uint64_t pol_b = p.raster == 0 ? l2_policy_evict_first() : l2_policy_evict_last();
             uint32_t fills = 0;
-            bool ok = true;
+            bool ok = p.withhold_loads == 0;  // the failure-path self-test withholds every load
             for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step) {
                 int mb, nb;
                 tile_coords(tile, p, mb, nb);
@@ -205,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < p.num_k; ++kb, ++fills) {
                     const uint32_t s = fills % S;
                     const uint32_t ph = (fills / S) & 1u;
-                    if (!wait_bounded(empty_bar(s), ph ^ 1u, p.err, kErrProducerWait)) {
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, p, kErrProducerWait)) {
                         ok = false;
                         break;
                     }
@@ -239,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t outstanding = fills < uint32_t(S) ? fills : uint32_t(S);
                 for (uint32_t j = 0; j < outstanding; ++j) {
                     const uint32_t f = fills - 1 - j;
-                    wait_bounded(full_bar(f % S), (f / S) & 1u, p.err, kErrDrainWait, false);
+                    wait_bounded(full_bar(f % S), (f / S) & 1u, p, kErrDrainWait, false);
                 }
             }
         }
@@ -253,13 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step, ++it) {
                 const uint32_t acc = it & 1;
                 const uint32_t acc_ph = (it >> 1) & 1;
-                if (!wait_bounded(tempty_bar(acc), acc_ph ^ 1u, p.err, kErrMmaWaitTmem)) break;
+                if (!wait_bounded(tempty_bar(acc), acc_ph ^ 1u, p, kErrMmaWaitTmem)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBlockN;
                 for (int kb = 0; kb < p.num_k; ++kb, ++fills) {
                     const uint32_t s = fills % S;
                     const uint32_t ph = (fills / S) & 1u;
-                    if (!wait_bounded(full_bar(s), ph, p.err, kErrMmaWaitFull)) {
+                    if (!wait_bounded(full_bar(s), ph, p, kErrMmaWaitFull)) {
                         ok = false;
                         break;
                     }
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The MMAs must complete before TMEM is freed (in both CTAs).
             if constexpr (PAIR) umma_commit_pair(drain_bar, 0x3);
             else umma_commit(drain_bar);
-            wait_bounded(drain_bar, 0, p.err, kErrDrainWait, false);
+            wait_bounded(drain_bar, 0, p, kErrDrainWait, false);
         }
     } else if (warp >= kFirstEpilogueWarp) {
         // ---------------- epilogue (each CTA stores its own 128 rows) ----------------
@@ -314,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int nchunks = 0;
             if (row0 < p.m_dim)  // warp-uniform
                 while (nchunks * kChunk < kBlockN && n0 + nchunks * kChunk < p.n_dim) ++nchunks;
-            if (!warp_wait(tfull_bar(acc), acc_ph, p.err, kErrEpilogueWait, lane)) break;
+            if (!warp_wait(tfull_bar(acc), acc_ph, p, kErrEpilogueWait, lane)) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * kBlockN;
             if constexpr (OUT_F32) {
@@ -424,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // The second CTA of a pair has not watched the MMAs: wait for the
         // drain commit that the first CTA multicast to it.
-        if (PAIR && !leader) wait_bounded(drain_bar, 0, p.err, kErrDrainWait, false);
+        if (PAIR && !leader) wait_bounded(drain_bar, 0, p, kErrDrainWait, false);
         tmem_dealloc<PAIR>(tmem_base, kTmemCols);
     }
 }
@@ -591,7 +598,9 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     kp.d = g.d;
     kp.ldd = g.ldd;
     kp.accumulate = g.accumulate ? 1 : 0;
+    kp.withhold_loads = g.withhold_loads ? 1 : 0;
     kp.err = g.err;
+    kp.timeout_ns = g.timeout_ns;
     const int slots = pair ? num_sms / 2 : num_sms;
     const int units = kp.num_tiles < slots ? kp.num_tiles : slots;
     const int grid = pair ? 2 * units : units;

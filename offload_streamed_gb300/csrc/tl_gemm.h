@@ -32,6 +32,8 @@ struct GemmDesc {
     OutKind out = OutKind::BF16;
     bool accumulate = false;  // F32 only: D += A.B
     int32_t* err = nullptr;   // device word for bounded-wait timeouts
+    uint64_t timeout_ns = 2000000000ull;  // limit of every bounded wait
+    bool withhold_loads = false;  // failure-path self-test: the producer issues no loads
 };
 
 // Shape / alignment rules shared by the launcher and the ABI checks.

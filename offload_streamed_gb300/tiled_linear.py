@@ -94,6 +94,8 @@ def load():
         L.tiled_linear_gemm_dw.restype = st
         L.tiled_linear_gemm_dx.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp, vp]
         L.tiled_linear_gemm_dx.restype = st
+        L.tiled_linear_selftest_timeout.argtypes = [vp, sz, i64, vp]
+        L.tiled_linear_selftest_timeout.restype = st
         L.tiled_linear_forward_static.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp]
         L.tiled_linear_forward_static.restype = st
         L.tiled_linear_host_alloc.argtypes = [sz, ctypes.POINTER(vp)]
@@ -173,6 +175,13 @@ def tiled_linear_gemm_dw(T, K, n, x, ldx, dy, lddy, dw, lddw, err, stream) -> No
 def tiled_linear_gemm_dx(T, K, n, dy, lddy, w, ldw, dx, lddx, accumulate, err, stream) -> None:
     _check(load().tiled_linear_gemm_dx(T, K, n, dy, lddy, w, ldw, dx, lddx, int(accumulate), err, stream),
            "tiled_linear_gemm_dx")
+
+
+def tiled_linear_selftest_timeout(scratch_dev: int, scratch_bytes: int, timeout_ns: int, stream: int) -> None:
+    """Run the kernels' failure path once (see the header); the error bits
+    land in the first int32 of scratch_dev."""
+    _check(load().tiled_linear_selftest_timeout(scratch_dev, scratch_bytes, timeout_ns, stream),
+           "tiled_linear_selftest_timeout")
 
 
 def tiled_linear_forward_static(T, K, M, N, w_host, x_dev, y_dev, status_host, stream) -> None:
