@@ -63,11 +63,15 @@ typedef enum { TL_LAYOUT_ROW_MAJOR = 0, TL_LAYOUT_TILE_MAJOR = 1 } tl_layout;
 
 /* Timings from CUDA events the library records on the streams that run the
  * work, in milliseconds.  The first block describes the LAST forward and
- * backward call: *_gemm_ms are sums over the tiles of each kernel's own span
- * on the compute stream, *_h2d_ms / *_d2h_ms sums of the copy spans on the
- * copy streams, *_total_ms the whole call on `stream`.  The sum_* block adds
- * the same quantities over every call since the handle was created or
- * tiled_linear_reset_stats was called (fwd_calls / bwd_calls of them). */
+ * backward call: *_gemm_ms are sums of the kernels' own spans on the compute
+ * stream, *_h2d_ms / *_d2h_ms sums of the copy spans on the copy streams,
+ * *_total_ms the whole call on `stream`.  The sum_* block adds the same
+ * quantities over every call since the handle was created or
+ * tiled_linear_reset_stats was called (fwd_calls / bwd_calls of them).
+ * persistent = 1: each pass ran as ONE persistent launch (fwd_launches =
+ * bwd_launches = 1); the backward launch runs both GEMMs, so bwd_gemm_ms is
+ * its span and bwd_dw_gemm_ms / bwd_dx_gemm_ms are 0.  persistent = 0: one
+ * launch per tile and GEMM; bwd_gemm_ms = bwd_dw_gemm_ms + bwd_dx_gemm_ms. */
 typedef struct {
     int32_t n_tiles;
     int32_t depth;            /* d used by the call                           */
@@ -81,11 +85,14 @@ typedef struct {
     int64_t fwd_calls, bwd_calls;
     double sum_fwd_total_ms, sum_fwd_gemm_ms, sum_fwd_h2d_ms;
     double sum_bwd_total_ms, sum_bwd_dw_gemm_ms, sum_bwd_dx_gemm_ms, sum_bwd_h2d_ms, sum_bwd_d2h_ms;
+    double sum_bwd_gemm_ms;
+    float bwd_gemm_ms;
+    int32_t persistent;
 } tl_stats;
 
 /* Device workspace bytes needed for (K, M, N, d): (min(d,N-1)+1) weight slots
- * and min(2,N) gradient staging slots of K*(M/N) bf16 each, plus a 4 KiB
- * header.  d = -1 (automatic depth) sizes for d = min(N-1, 3).  Returns 0 if
+ * and min(2,N) gradient staging slots of K*(M/N) bf16 each, plus a 64 KiB
+ * header (error word, copy-stream flags and per-tile progress counters).  d = -1 (automatic depth) sizes for d = min(N-1, 3).  Returns 0 if
  * the arguments are invalid. */
 size_t tiled_linear_workspace_bytes(int64_t K, int64_t M, int32_t N, int32_t d);
 
@@ -105,6 +112,13 @@ size_t tiled_linear_workspace_bytes(int64_t K, int64_t M, int32_t N, int32_t d);
  *  workspace_dev, workspace_bytes: device memory, 256-byte aligned, at least
  *            tiled_linear_workspace_bytes(K, M, N, d); owned by the caller,
  *            used until tiled_linear_destroy returns.
+ * Execution mode: by default each call launches one GEMM per tile (and per
+ * GEMM in the backward), ordered against the copy streams by CUDA events.
+ * With the environment variable TILED_LINEAR_PERSISTENT=1 at creation time,
+ * and when the shapes allow it (Mi % 256 == 0, d + 1 <= 8, N <= 4096) and
+ * the driver's stream memory operations work, each pass instead runs as ONE
+ * persistent launch that waits for and releases ring slots through 32-bit
+ * flags in the workspace header (tl_stats.persistent reports the mode).
  * Errors: TL_ERR_INVALID (shapes/pointers), TL_ERR_NOT_PINNED,
  * TL_ERR_WORKSPACE, TL_ERR_CUDA.  On error *out is set to NULL. */
 tl_status tiled_linear_create(tl_handle **out, int64_t K, int64_t M, int32_t N, int32_t d,
@@ -128,7 +142,8 @@ tl_status tiled_linear_forward(tl_handle *h, int64_t T, const void *x_dev, void 
 /* Backward, tiles in descending order i = N-1 .. 0:
  *   dW_i = X^T . dY_i  (fp32 accumulation, bf16 RNE) -> dw_host tile i
  *   dx_dev[T, K] (fp32, ld K) = sum_i dY_i . W_i^T   (overwritten: the first
- *   tile stores, later tiles add, in this fixed order)
+ *   tile stores, later tiles add, in this fixed order; the persistent mode
+ *   sums two consecutive tiles in one fp32 accumulator before each add)
  * dy_dev is [T, M] bf16 (ld M).  T = 0 writes dW = 0.  dW on the host is
  * complete once `stream` has completed.  Errors as tiled_linear_forward. */
 tl_status tiled_linear_backward(tl_handle *h, int64_t T, const void *x_dev,

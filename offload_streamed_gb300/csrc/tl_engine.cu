@@ -23,19 +23,55 @@
 #include "tiled_linear.h"
 #include "tl_gemm.h"
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
 
 namespace {
 
-constexpr size_t kHeaderBytes = 4096;
+// Workspace header: the kernels' error word, then the persistent pass's
+// sequence flags and per-position counters (zeroed per call).
+constexpr size_t kHeaderBytes = 65536;
+constexpr size_t kFlagsOffset = 256;
+constexpr size_t kDoneOffset = 4096;
+constexpr size_t kDwDoneOffset = kDoneOffset + 4 * size_t(tl::kMaxPassTiles);
+constexpr size_t kDxDoneOffset = kDwDoneOffset + 4 * size_t(tl::kMaxPassTiles);
+static_assert(kDxDoneOffset + 4 * size_t(tl::kMaxPassTiles) <= kHeaderBytes, "header layout");
+
+// Stream memory operations (copy streams <-> persistent pass kernel).
+using StreamValueFn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+struct MemOps {
+    StreamValueFn write = nullptr, wait = nullptr;
+};
+const MemOps& memops() {
+    static MemOps m;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            m.write = reinterpret_cast<StreamValueFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            m.wait = reinterpret_cast<StreamValueFn>(p);
+    });
+    return m;
+}
+constexpr unsigned kWaitGeq = 0x0;       // CU_STREAM_WAIT_VALUE_GEQ
+constexpr unsigned kWriteDefault = 0x0;  // CU_STREAM_WRITE_VALUE_DEFAULT
 constexpr size_t kAlign = 256;
 constexpr int kMaxStage = 2;
 constexpr int kAutoMaxDepth = 3;
@@ -77,6 +113,7 @@ struct CallSlot {
     std::vector<cudaEvent_t> ev[8];
     bool pending = false;  // recorded, not yet harvested
     bool harvested = false;
+    int32_t nk = 0;        // kernel spans recorded (N per-tile launches, or 1 pass)
     int32_t depth = 0, launches = 0;
     int64_t h2d_bytes = 0, d2h_bytes = 0;
     float total = 0, gemm1 = 0, gemm2 = 0, h2d = 0, d2h = 0;
@@ -113,6 +150,13 @@ struct tl_handle {
     std::vector<cudaEvent_t> ev_ready, ev_free, ev_dwdone, ev_drained;
     uint64_t fetch_seq = 0, stage_seq = 0;
     int num_sms = 0;
+    bool persistent = false;  // whole passes as one persistent launch
+    uint32_t* flags = nullptr;
+    uint32_t* done = nullptr;
+    uint32_t* dwdone = nullptr;
+    uint32_t* dxdone = nullptr;
+    cudaEvent_t ev_d2h_tail = nullptr;  // last dW write-back of the last backward call
+    cudaEvent_t ev_call_done = nullptr; // end of the last call (calls share the pass counters)
     Phase fwd, bwd;
     tl_status sticky = TL_OK;
     std::string msg;
@@ -145,6 +189,13 @@ tl_status fail(tl_handle* h, tl_status st, const std::string& what) {
         cudaError_t e_ = (call);                                                          \
         if (e_ != cudaSuccess)                                                            \
             return fail((h), TL_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+    } while (0)
+
+#define TL_CU(h, call)                                                                     \
+    do {                                                                                   \
+        CUresult r_ = (call);                                                              \
+        if (r_ != CUDA_SUCCESS)                                                            \
+            return fail((h), TL_ERR_CUDA, std::string(#call) + ": CUresult " + std::to_string(int(r_))); \
     } while (0)
 
 bool is_pinned_host(const void* p) {
@@ -250,12 +301,12 @@ tl_status harvest(tl_handle* h, Phase& p, CallSlot& c, int n) {
     c.total = span_ms(c.start, c.end);
     c.gemm1 = c.gemm2 = c.h2d = c.d2h = 0;
     for (int i = 0; i < n; ++i) {
-        c.gemm1 += span_ms(c.ev[0][i], c.ev[1][i]);
-        c.h2d += span_ms(c.ev[4][i], c.ev[5][i]);
-        if (p.backward) {
-            c.gemm2 += span_ms(c.ev[2][i], c.ev[3][i]);
-            c.d2h += span_ms(c.ev[6][i], c.ev[7][i]);
+        if (i < c.nk) {
+            c.gemm1 += span_ms(c.ev[0][i], c.ev[1][i]);
+            if (p.backward && c.nk == n) c.gemm2 += span_ms(c.ev[2][i], c.ev[3][i]);
         }
+        c.h2d += span_ms(c.ev[4][i], c.ev[5][i]);
+        if (p.backward) c.d2h += span_ms(c.ev[6][i], c.ev[7][i]);
     }
     c.pending = false;
     c.harvested = true;
@@ -304,11 +355,76 @@ tl_status finish_auto_depth(tl_handle* h) {
     dnew = std::max<int32_t>(1, std::min<int32_t>(dnew, h->slot_cap - 1));
     if (h->slot_cap - 1 < 1) dnew = 0;
     if (dnew != h->d) {
-        for (int s = 0; s < h->slot_cap; ++s) TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[s], 0));
+        if (h->persistent) {
+            // Every earlier fetch has been consumed (the first forward call has
+            // finished); mark every slot free up to the next fetch so that the
+            // new ring size starts clean.
+            TL_TRY(h, cudaStreamSynchronize(h->h2d));
+            for (int s = 0; s < tl::kMaxPassSlots; ++s)
+                TL_CU(h, memops().write(reinterpret_cast<CUstream>(h->h2d),
+                                        reinterpret_cast<CUdeviceptr>(h->flags + tl::kFlagFreed + s),
+                                        uint32_t(h->fetch_seq), kWriteDefault));
+        } else {
+            for (int s = 0; s < h->slot_cap; ++s) TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[s], 0));
+            h->fetch_seq = 0;
+        }
         h->d = dnew;
-        h->fetch_seq = 0;
     }
     h->auto_pending = false;
+    return TL_OK;
+}
+
+// ---- persistent passes ------------------------------------------------------
+CUstream cu(cudaStream_t s) { return reinterpret_cast<CUstream>(s); }
+CUdeviceptr cuptr(const void* p) { return reinterpret_cast<CUdeviceptr>(p); }
+
+tl::PassDesc pass_desc(const tl_handle* h, bool backward, int64_t T, uint64_t fetch_base, uint64_t stage_base) {
+    tl::PassDesc d;
+    d.backward = backward;
+    d.T = T;
+    d.K = h->s.K;
+    d.Mi = h->s.Mi;
+    d.N = h->s.N;
+    d.nslots = h->d + 1;
+    for (int i = 0; i < d.nslots && i < tl::kMaxPassSlots; ++i) d.slots[i] = h->slot[i];
+    d.nstage = h->nstage;
+    for (int g = 0; g < d.nstage && g < tl::kMaxPassStages; ++g) d.stages[g] = h->stage[g];
+    d.fetch_base = uint32_t(fetch_base);
+    d.stage_base = uint32_t(stage_base);
+    // dX is accumulated over groups of two tiles (one dX read-modify-write
+    // per two tiles) whenever the ring holds two tiles.
+    d.dx_group = d.nslots >= 2 ? 2 : 1;
+    d.flags = h->flags;
+    d.done = h->done;
+    d.dwdone = h->dwdone;
+    d.dxdone = h->dxdone;
+    d.err = h->err_dev;
+    return d;
+}
+
+// Host->device fetches of the pass's tiles, in pass order, gated by the
+// slots' "freed" flags and announced by "ready" flags.
+tl_status enqueue_fetches(tl_handle* h, CallSlot& t, uint64_t base, bool backward) {
+    const MemOps& mo = memops();
+    const int N = h->s.N;
+    const uint64_t nslots = uint64_t(h->d + 1);
+    for (int j = 0; j < N; ++j) {
+        const int i = backward ? N - 1 - j : j;
+        const uint64_t f = base + uint64_t(j);
+        const int sl = int(f % nslots);
+        if (f >= nslots)
+            TL_CU(h, mo.wait(cu(h->h2d), cuptr(h->flags + tl::kFlagFreed + sl), uint32_t(f - nslots + 1), kWaitGeq));
+        TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
+        TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
+        TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
+        TL_CU(h, mo.write(cu(h->h2d), cuptr(h->flags + tl::kFlagReady + sl), uint32_t(f + 1), kWriteDefault));
+    }
+    return TL_OK;
+}
+
+tl_status launch_pass(tl_handle* h, const tl::PassDesc& d, cudaStream_t cs) {
+    std::string why;
+    if (tl::pass_launch(d, h->num_sms, cs, &why) != cudaSuccess) return fail(h, TL_ERR_CUDA, "pass launch: " + why);
     return TL_OK;
 }
 
@@ -387,11 +503,15 @@ tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t 
     h->d = h->slot_cap - 1;
     h->auto_pending = (d < 0);
     h->err_dev = reinterpret_cast<int32_t*>(h->ws);
+    h->flags = reinterpret_cast<uint32_t*>(h->ws + kFlagsOffset);
+    h->done = reinterpret_cast<uint32_t*>(h->ws + kDoneOffset);
+    h->dwdone = reinterpret_cast<uint32_t*>(h->ws + kDwDoneOffset);
+    h->dxdone = reinterpret_cast<uint32_t*>(h->ws + kDxDoneOffset);
     uint8_t* p = h->ws + kHeaderBytes;
     for (int s = 0; s < h->slot_cap; ++s, p += tb) h->slot.push_back(p);
     for (int g = 0; g < h->nstage; ++g, p += tb) h->stage.push_back(p);
 
-    if (cudaMemset(h->err_dev, 0, sizeof(int32_t)) != cudaSuccess ||
+    if (cudaMemset(h->ws, 0, kHeaderBytes) != cudaSuccess ||
         cudaHostAlloc(reinterpret_cast<void**>(&h->err_mirror), sizeof(int32_t), cudaHostAllocPortable) !=
             cudaSuccess) {
         h->msg = std::string("error-word setup: ") + cudaGetErrorString(cudaGetLastError());
@@ -420,7 +540,129 @@ tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t 
         h->msg = "cudaDeviceGetAttribute(multiProcessorCount) failed";
         return bail(TL_ERR_CUDA);
     }
+    if (cudaEventCreateWithFlags(&h->ev_d2h_tail, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_call_done, cudaEventDisableTiming) != cudaSuccess) {
+        h->msg = "event creation failed";
+        return bail(TL_ERR_CUDA);
+    }
+    // One launch per tile and per GEMM by default (the faster mode on the
+    // GPT-scale layer: the separate dW and dX launches keep their operand
+    // pairs L2-resident).  TILED_LINEAR_PERSISTENT=1 asks for whole passes as
+    // one persistent launch, granted when the stream memory operations are
+    // there and the shapes allow it (tile width a multiple of 256, at most 8
+    // ring slots).
+    {
+        const char* env = std::getenv("TILED_LINEAR_PERSISTENT");
+        const bool wanted = env && env[0] == '1';
+        tl::PassDesc probe = pass_desc(h, false, 1, 0, 0);
+        probe.nslots = h->slot_cap;
+        probe.x = h->ws;
+        probe.y = h->ws;
+        const MemOps& mo = memops();
+        if (wanted && mo.write && mo.wait && tl::pass_check(probe, h->num_sms).empty()) {
+            // the stream memory operations must work on this device
+            if (mo.write(cu(h->h2d), cuptr(h->flags + tl::kNumFlags), 0u, kWriteDefault) == CUDA_SUCCESS &&
+                cudaStreamSynchronize(h->h2d) == cudaSuccess && tl::pass_preload() == cudaSuccess)
+                h->persistent = true;
+            cudaGetLastError();
+        }
+    }
     *out = h;
+    return TL_OK;
+}
+
+// Forward as one persistent pass.  The caller's stream first waits for the
+// handle's previous call (the pass counters are reused), then the counters of
+// this pass are cleared and the kernel launched; the fetches run ahead on the
+// h2d stream as far as the ring's "freed" flags allow.
+tl_status forward_persistent(tl_handle* h, int64_t T, const void* x, void* y, cudaStream_t cs) {
+    tl_status st;
+    CallSlot* tp = begin_call(h, h->fwd, &st);
+    if (!tp) return st;
+    CallSlot& t = *tp;
+    const Shape& s = h->s;
+    const uint64_t base = h->fetch_seq;
+    h->fetch_seq += uint64_t(s.N);
+    TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_call_done, 0));
+    TL_TRY(h, cudaEventRecord(t.start, cs));
+    TL_TRY(h, cudaMemsetAsync(h->done, 0, 4 * size_t(s.N), cs));
+    // The kernel is launched before its fetches are queued: every flag wait
+    // a copy stream holds must be satisfiable by a kernel already launched.
+    tl::PassDesc d = pass_desc(h, false, T, base, 0);
+    d.x = x;
+    d.y = y;
+    TL_TRY(h, cudaEventRecord(t.ev[0][0], cs));
+    if ((st = launch_pass(h, d, cs)) != TL_OK) return st;
+    TL_TRY(h, cudaEventRecord(t.ev[1][0], cs));
+    if ((st = enqueue_fetches(h, t, base, false)) != TL_OK) return st;
+    TL_TRY(h, cudaEventRecord(t.end, cs));
+    TL_TRY(h, cudaEventRecord(h->ev_call_done, cs));
+    TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    t.nk = 1;
+    t.depth = h->d;
+    t.launches = 1;
+    t.h2d_bytes = int64_t(s.N) * int64_t(tile_bytes(s.K, s.Mi));
+    t.d2h_bytes = 0;
+    end_call(h->fwd, t);
+    return TL_OK;
+}
+
+// Backward as one persistent pass; the dW write-backs are queued on the d2h
+// stream, each gated by its staging slot's "dwready" flag, and the caller's
+// stream waits for the last one.
+tl_status backward_persistent(tl_handle* h, int64_t T, const void* x, const void* dy, float* dx,
+                              cudaStream_t cs) {
+    tl_status st;
+    const Shape& s = h->s;
+    const size_t tb = tile_bytes(s.K, s.Mi);
+    if (T == 0) {  // dW = X^T dY over an empty sum: zero
+        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_call_done, 0));
+        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_d2h_tail, 0));
+        TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tb, cs));
+        for (int i = 0; i < s.N; ++i) TL_TRY(h, copy_dw_tile(h, i, h->stage[0], cs));
+        TL_TRY(h, cudaEventRecord(h->ev_call_done, cs));
+        return TL_OK;
+    }
+    CallSlot* tp = begin_call(h, h->bwd, &st);
+    if (!tp) return st;
+    CallSlot& t = *tp;
+    const MemOps& mo = memops();
+    const uint64_t base = h->fetch_seq;
+    h->fetch_seq += uint64_t(s.N);
+    const uint64_t sbase = h->stage_seq;
+    h->stage_seq += uint64_t(s.N);
+    TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_call_done, 0));
+    TL_TRY(h, cudaEventRecord(t.start, cs));
+    TL_TRY(h, cudaMemsetAsync(h->done, 0, (kDxDoneOffset - kDoneOffset) + 4 * size_t(s.N), cs));
+    tl::PassDesc d = pass_desc(h, true, T, base, sbase);
+    d.x = x;
+    d.dy = dy;
+    d.dx = dx;
+    TL_TRY(h, cudaEventRecord(t.ev[0][0], cs));
+    if ((st = launch_pass(h, d, cs)) != TL_OK) return st;
+    TL_TRY(h, cudaEventRecord(t.ev[1][0], cs));
+    if ((st = enqueue_fetches(h, t, base, true)) != TL_OK) return st;
+    for (int j = 0; j < s.N; ++j) {
+        const int i = s.N - 1 - j;
+        const uint64_t sj = sbase + uint64_t(j);
+        const int g = int(sj % uint64_t(h->nstage));
+        TL_CU(h, mo.wait(cu(h->d2h), cuptr(h->flags + tl::kFlagDwReady + g), uint32_t(sj + 1), kWaitGeq));
+        TL_TRY(h, cudaEventRecord(t.ev[6][j], h->d2h));
+        TL_TRY(h, copy_dw_tile(h, i, h->stage[g], h->d2h));
+        TL_TRY(h, cudaEventRecord(t.ev[7][j], h->d2h));
+        TL_CU(h, mo.write(cu(h->d2h), cuptr(h->flags + tl::kFlagDrained + g), uint32_t(sj + 1), kWriteDefault));
+    }
+    TL_TRY(h, cudaEventRecord(h->ev_d2h_tail, h->d2h));
+    TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_d2h_tail, 0));
+    TL_TRY(h, cudaEventRecord(t.end, cs));
+    TL_TRY(h, cudaEventRecord(h->ev_call_done, cs));
+    TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    t.nk = 1;
+    t.depth = h->d;
+    t.launches = 1;
+    t.h2d_bytes = int64_t(s.N) * int64_t(tb);
+    t.d2h_bytes = int64_t(s.N) * int64_t(tb);
+    end_call(h->bwd, t);
     return TL_OK;
 }
 
@@ -461,6 +703,7 @@ tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void*
     if ((st = finish_auto_depth(h)) != TL_OK) return st;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (h->persistent) return forward_persistent(h, T, x_dev, y_dev, cs);
     const Shape& s = h->s;
     CallSlot* tp = begin_call(h, h->fwd, &st);
     if (!tp) return st;
@@ -497,6 +740,7 @@ tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void*
     }
     TL_TRY(h, cudaEventRecord(t.end, cs));
     TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    t.nk = s.N;
     t.depth = h->d;
     t.launches = s.N;
     t.h2d_bytes = int64_t(s.N) * int64_t(tile_bytes(s.K, s.Mi));
@@ -519,6 +763,7 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     if ((st = finish_auto_depth(h)) != TL_OK) return st;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (h->persistent) return backward_persistent(h, T, x_dev, dy_dev, dx_dev, cs);
     const Shape& s = h->s;
     const size_t tb = tile_bytes(s.K, s.Mi);
 
@@ -600,6 +845,7 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     for (int g = 0; g < h->nstage; ++g) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[g], 0));
     TL_TRY(h, cudaEventRecord(t.end, cs));
     TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    t.nk = s.N;
     t.depth = h->d;
     t.launches = 2 * s.N;
     t.h2d_bytes = int64_t(s.N) * int64_t(tb);
@@ -627,6 +873,8 @@ tl_status tiled_linear_destroy(tl_handle* h) {
                 if (c.end) cudaEventSynchronize(c.end);
         destroy_phase(h->fwd);
         destroy_phase(h->bwd);
+        if (h->ev_d2h_tail) cudaEventDestroy(h->ev_d2h_tail);
+        if (h->ev_call_done) cudaEventDestroy(h->ev_call_done);
         if (h->h2d) cudaStreamDestroy(h->h2d);
         if (h->d2h) cudaStreamDestroy(h->d2h);
         if (h->err_mirror) cudaFreeHost(h->err_mirror);
@@ -666,8 +914,9 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
         const CallSlot& c = h->bwd.ring[h->bwd.last];
         out->bwd_valid = 1;
         out->bwd_total_ms = c.total;
-        out->bwd_dw_gemm_ms = c.gemm1;
-        out->bwd_dx_gemm_ms = c.gemm2;
+        out->bwd_gemm_ms = c.gemm1 + c.gemm2;
+        out->bwd_dw_gemm_ms = c.nk == h->s.N ? c.gemm1 : 0.f;
+        out->bwd_dx_gemm_ms = c.nk == h->s.N ? c.gemm2 : 0.f;
         out->bwd_h2d_ms = c.h2d;
         out->bwd_d2h_ms = c.d2h;
         out->bwd_wait_ms = c.total - c.gemm1 - c.gemm2;
@@ -685,6 +934,8 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
     out->sum_bwd_dx_gemm_ms = h->bwd.sum_gemm2;
     out->sum_bwd_h2d_ms = h->bwd.sum_h2d;
     out->sum_bwd_d2h_ms = h->bwd.sum_d2h;
+    out->sum_bwd_gemm_ms = h->bwd.sum_gemm1 + h->bwd.sum_gemm2;
+    out->persistent = h->persistent ? 1 : 0;
     int32_t word = 0;
     TL_TRY(h, cudaMemcpy(&word, h->err_dev, sizeof(word), cudaMemcpyDeviceToHost));
     if (word != 0)

@@ -22,9 +22,8 @@
 // TMA loads to land, the MMA thread for its own MMAs, and TMEM is freed
 // before the CTA exits.
 #include "tl_gemm.h"
-#include "tl_ptx.cuh"
+#include "tl_kernel_common.cuh"
 
-#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -35,44 +34,12 @@
 namespace tl {
 namespace {
 
-constexpr int kUmmaK = 16;
-constexpr uint32_t kStageA = kBlockM * kBlockK * 2;  // 128 rows of A per CTA: 16 KiB
-constexpr uint32_t kMnChunk = 64 * kBlockK * 2;      // 64 MN elements x 64 K rows = 8 KiB
-constexpr uint32_t kTmemCols = 2 * kBlockN;          // two fp32 accumulators of 256 columns
-constexpr int kThreads = 256;
-constexpr int kFirstEpilogueWarp = 4;
-// Epilogue staging: each of the 4 epilogue warps owns a few boxes of 32
-// output rows x 128 bytes (32 fp32 or 64 bf16 columns) for its TMA traffic.
-constexpr uint32_t kEpiBuf = 32 * 128;
-constexpr uint32_t kBarBytes = 512;
-
-static_assert(kBlockK * 2 == 128, "one K-block row must be one 128-byte swizzle row");
-
-// Tile geometry.  Single CTA: 128 x 256 output tile, B = 256 rows of N per
-// stage.  CTA pair (cta_group::2): 256 x 256 output tile; each CTA loads its
-// own 128 rows of A and its own 128 rows (N) of B, and the pair's MMA reads
-// both CTAs' shared memory.
-// bf16 outputs leave through TMA stores of 128B-swizzled staging boxes (2
-// per epilogue warp); fp32 outputs (dX, possibly accumulated) are written by
-// the epilogue threads directly, which keeps shared-memory bandwidth for the
-// tensor cores' operand reads.
-template <bool PAIR, bool OUT_F32>
-struct Geo {
-    static constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;
-    static constexpr int kBRows = PAIR ? kBlockN / 2 : kBlockN;
-    static constexpr uint32_t kStageB = uint32_t(kBRows) * kBlockK * 2;
-    static constexpr uint32_t kStageBytes = kStageA + kStageB;
-    static constexpr int kEpiBoxes = OUT_F32 ? 0 : 2;
-    static constexpr uint32_t kEpiBytes = 4u * kEpiBoxes * kEpiBuf;
-    static constexpr int kStages = PAIR ? 6 : 4;
-    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + kEpiBytes + kBarBytes + 1024;
-    static_assert(kSmem <= 232448, "shared memory budget");
-};
+using namespace kc;
 
 struct KParams {
     int32_t m_dim, n_dim, k_dim;
     int32_t num_m, num_n, num_k, num_tiles;
-    int32_t raster, group;  // raster 0: groups of `group` m-blocks (m fastest); 1: groups of n-blocks
+    int32_t raster, group;  // tile order (see kc::tile_coords)
     void* d;
     int64_t ldd;
     int32_t accumulate;
@@ -81,74 +48,12 @@ struct KParams {
     uint64_t timeout_ns;
 };
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int32_t* err, int32_t code,
-                                       bool stop_on_error, uint64_t timeout_ns) {
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 0) {
-            if (stop_on_error && *reinterpret_cast<volatile int32_t*>(err) != 0) return false;
-            if (global_timer_ns() - t0 > timeout_ns) {
-                atomicOr(err, code);
-                return false;
-            }
-        }
-    }
-}
-
-// The MMA thread's waits use the base limit; the producer's wait for a free
-// stage and the epilogue's wait for an accumulator (both downstream of the
-// MMA thread) use twice that, so when a pipeline stalls the role nearest the
-// stall reports first.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const KParams& p, int32_t code,
-                                             bool stop_on_error = true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const bool downstream = code == kErrProducerWait || code == kErrEpilogueWait;
-    return wait_slow(bar, parity, p.err, code, stop_on_error, downstream ? 2 * p.timeout_ns : p.timeout_ns);
-}
-
-// Warp-uniform wait: lane 0 waits (bounded); then every lane observes the
-// completed phase itself, which cannot move on before this warp arrives.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const KParams& p, int32_t code,
-                                          int lane) {
-    int32_t* err = p.err;
-    int ok = 1;
-    if (lane == 0) ok = wait_bounded(bar, parity, p, code) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) return false;
-    int mine = 0;
-    for (int n = 0; n < (1 << 20) && !mine; ++n) mine = mbar_try_wait(bar, parity) ? 1 : 0;
-    if (!mine) atomicOr(err, code);
-    return __all_sync(0xffffffffu, mine) != 0;
-}
-
-// Output tile order: groups of `group` blocks along one dimension, walking
-// the other dimension inside the group, so that the group's blocks of one
-// operand stay in L2 while the other operand streams past once per group.
-__device__ __forceinline__ void tile_coords(int tile, const KParams& p, int& mb, int& nb) {
-    const int outer = p.raster == 0 ? p.num_m : p.num_n;
-    const int inner = p.raster == 0 ? p.num_n : p.num_m;
-    const int group_tiles = p.group * inner;
-    const int g = tile / group_tiles;
-    const int first = g * p.group;
-    const int width = min(p.group, outer - first);
-    const int local = tile - g * group_tiles;
-    const int a = first + local % width;
-    const int b = local / width;
-    mb = p.raster == 0 ? a : b;
-    nb = p.raster == 0 ? b : a;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
 template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const __grid_constant__ CUtensorMap map_d, const KParams p) {
-    using G = Geo<PAIR, OUT_F32>;
+    using G = Geo<PAIR, OUT_F32 ? 0 : 2>;
+    const WaitCtx wc{p.err, p.timeout_ns};
     constexpr int S = G::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -206,13 +111,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = p.withhold_loads == 0;  // the failure-path self-test withholds every load
             for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step) {
                 int mb, nb;
-                tile_coords(tile, p, mb, nb);
+                tile_coords(tile, p.num_m, p.num_n, p.raster, p.group, mb, nb);
                 const int m0 = mb * G::kTileM + int(rank) * kBlockM;
                 const int n0 = nb * kBlockN + int(rank) * (PAIR ? G::kBRows : 0);
                 for (int kb = 0; kb < p.num_k; ++kb, ++fills) {
                     const uint32_t s = fills % S;
                     const uint32_t ph = (fills / S) & 1u;
-                    if (!wait_bounded(empty_bar(s), ph ^ 1u, p, kErrProducerWait)) {
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, kErrProducerWait)) {
                         ok = false;
                         break;
                     }
@@ -246,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t outstanding = fills < uint32_t(S) ? fills : uint32_t(S);
                 for (uint32_t j = 0; j < outstanding; ++j) {
                     const uint32_t f = fills - 1 - j;
-                    wait_bounded(full_bar(f % S), (f / S) & 1u, p, kErrDrainWait, false);
+                    wait_bounded(full_bar(f % S), (f / S) & 1u, wc, kErrDrainWait, false);
                 }
             }
         }
@@ -260,13 +165,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step, ++it) {
                 const uint32_t acc = it & 1;
                 const uint32_t acc_ph = (it >> 1) & 1;
-                if (!wait_bounded(tempty_bar(acc), acc_ph ^ 1u, p, kErrMmaWaitTmem)) break;
+                if (!wait_bounded(tempty_bar(acc), acc_ph ^ 1u, wc, kErrMmaWaitTmem)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBlockN;
                 for (int kb = 0; kb < p.num_k; ++kb, ++fills) {
                     const uint32_t s = fills % S;
                     const uint32_t ph = (fills / S) & 1u;
-                    if (!wait_bounded(full_bar(s), ph, p, kErrMmaWaitFull)) {
+                    if (!wait_bounded(full_bar(s), ph, wc, kErrMmaWaitFull)) {
                         ok = false;
                         break;
                     }
@@ -275,10 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sb = sa + kStageA;
 #pragma unroll
                     for (int j = 0; j < kBlockK / kUmmaK; ++j) {
-                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + j * 2048, kMnChunk, 1024)
-                                                 : smem_desc_sw128(sa + j * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + j * 2048, kMnChunk, 1024)
-                                                 : smem_desc_sw128(sb + j * 32, 16, 1024);
+                        const uint64_t ad = operand_desc(A_MN, sa, j);
+                        const uint64_t bd = operand_desc(B_MN, sb, j);
                         if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                         else umma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                     }
@@ -293,18 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The MMAs must complete before TMEM is freed (in both CTAs).
             if constexpr (PAIR) umma_commit_pair(drain_bar, 0x3);
             else umma_commit(drain_bar);
-            wait_bounded(drain_bar, 0, p, kErrDrainWait, false);
+            wait_bounded(drain_bar, 0, wc, kErrDrainWait, false);
         }
     } else if (warp >= kFirstEpilogueWarp) {
         // ---------------- epilogue (each CTA stores its own 128 rows) ----------------
-        // Warp q owns TMEM lanes 32q..32q+31 = output rows row0..row0+31 of
-        // the CTA's half tile; lane l holds row row0 + l.
-        //  bf16: per 64-column chunk, two tcgen05.ld, pack, write the lane's
-        //    128-byte row into a 128B-swizzled staging box; one lane issues a
-        //    TMA store of the 32 x 64 box (double-buffered).
-        //  fp32: per 32-column chunk, tcgen05.ld and a direct 128-byte store of
-        //    the lane's row; when accumulating, the old values of the next
-        //    chunk are loaded while the current one is added and stored.
+        // bf16 outputs leave through TMA stores of swizzled staging boxes; fp32
+        // outputs (dX, possibly accumulated) are written by the threads
+        // directly, which keeps shared-memory bandwidth for the tensor cores.
         constexpr int kChunk = OUT_F32 ? 32 : 64;
         const int q = warp & 3;
         const uint32_t epi0 = smem0 + S * G::kStageBytes + uint32_t(q) * 2u * kEpiBuf;
@@ -315,104 +213,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc = it & 1;
             const uint32_t acc_ph = (it >> 1) & 1;
             int mb, nb;
-            tile_coords(tile, p, mb, nb);
+            tile_coords(tile, p.num_m, p.num_n, p.raster, p.group, mb, nb);
             const int row0 = mb * G::kTileM + int(rank) * kBlockM + q * 32;
             const int n0 = nb * kBlockN;
             int nchunks = 0;
             if (row0 < p.m_dim)  // warp-uniform
                 while (nchunks * kChunk < kBlockN && n0 + nchunks * kChunk < p.n_dim) ++nchunks;
-            if (!warp_wait(tfull_bar(acc), acc_ph, p, kErrEpilogueWait, lane)) break;
+            if (!warp_wait(tfull_bar(acc), acc_ph, wc, kErrEpilogueWait, lane)) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * kBlockN;
             if constexpr (OUT_F32) {
                 const int64_t row = int64_t(row0) + lane;
-                const bool row_ok = row < p.m_dim;
-                float* out_row = static_cast<float*>(p.d) + row * p.ldd + n0;
-                const bool rmw = p.accumulate != 0;
-                float4 old[8];
-                auto load_old = [&](int c, float4 (&dst)[8]) {
-                    const float* src = out_row + c * kChunk;
-                    const int rem = p.n_dim - (n0 + c * kChunk);
-                    if (row_ok && rem >= 32) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) dst[j] = reinterpret_cast<const float4*>(src)[j];
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            dst[j].x = (row_ok && 4 * j + 0 < rem) ? src[4 * j + 0] : 0.f;
-                            dst[j].y = (row_ok && 4 * j + 1 < rem) ? src[4 * j + 1] : 0.f;
-                            dst[j].z = (row_ok && 4 * j + 2 < rem) ? src[4 * j + 2] : 0.f;
-                            dst[j].w = (row_ok && 4 * j + 3 < rem) ? src[4 * j + 3] : 0.f;
-                        }
-                    }
-                };
-                if (rmw && nchunks > 0) load_old(0, old);
-                for (int c = 0; c < nchunks; ++c) {
-                    uint32_t w[32];
-                    tmem_ld_32cols(t_row + c * kChunk, w);
-                    float4 nxt[8];
-                    if (rmw && c + 1 < nchunks) load_old(c + 1, nxt);
-                    tmem_ld_wait();
-                    float4 val[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        val[j] = make_float4(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]),
-                                             __uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]));
-                        if (rmw) {
-                            val[j].x = old[j].x + val[j].x;
-                            val[j].y = old[j].y + val[j].y;
-                            val[j].z = old[j].z + val[j].z;
-                            val[j].w = old[j].w + val[j].w;
-                        }
-                    }
-                    float* dst = out_row + c * kChunk;
-                    const int rem = p.n_dim - (n0 + c * kChunk);
-                    if (row_ok && rem >= 32) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) reinterpret_cast<float4*>(dst)[j] = val[j];
-                    } else if (row_ok) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (4 * j + 0 < rem) dst[4 * j + 0] = val[j].x;
-                            if (4 * j + 1 < rem) dst[4 * j + 1] = val[j].y;
-                            if (4 * j + 2 < rem) dst[4 * j + 2] = val[j].z;
-                            if (4 * j + 3 < rem) dst[4 * j + 3] = val[j].w;
-                        }
-                    }
-                    if (rmw && c + 1 < nchunks) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) old[j] = nxt[j];
-                    }
-                }
+                epi_f32_direct(static_cast<float*>(p.d) + row * p.ldd + n0, row < p.m_dim, p.n_dim - n0, t_row,
+                               nchunks, p.accumulate != 0);
             } else {
-                for (int c = 0; c < nchunks; ++c) {
-                    uint32_t w[32];  // this lane's 128-byte row of the chunk (64 bf16)
-                    uint32_t v[32];
-                    tmem_ld_32cols(t_row + c * kChunk, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                    tmem_ld_32cols(t_row + c * kChunk + 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        w[16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                    const uint32_t sbuf = epi0 + buf * kEpiBuf;
-                    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used sbuf has read it
-                    __syncwarp();
-                    const uint32_t row_addr = sbuf + uint32_t(lane) * 128u;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_shared_v4(row_addr + ((uint32_t(j) ^ (uint32_t(lane) & 7u)) << 4), w[4 * j],
-                                     w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                    fence_proxy_async_shared();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&map_d, sbuf, n0 + c * kChunk, row0);
-                        bulk_commit_group();
-                    }
-                    buf ^= 1u;
-                }
+                epi_bf16_tma(&map_d, t_row, epi0, buf, nchunks, n0, row0, lane);
             }
             tc_fence_before();
             __syncwarp();
@@ -431,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // The second CTA of a pair has not watched the MMAs: wait for the
         // drain commit that the first CTA multicast to it.
-        if (PAIR && !leader) wait_bounded(drain_bar, 0, p, kErrDrainWait, false);
+        if (PAIR && !leader) wait_bounded(drain_bar, 0, wc, kErrDrainWait, false);
         tmem_dealloc<PAIR>(tmem_base, kTmemCols);
     }
 }
@@ -483,7 +298,7 @@ template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const KParams& kp,
                        int grid, cudaStream_t stream) {
     auto kern = gemm_kernel<A_MN, B_MN, OUT_F32, PAIR>;
-    constexpr size_t smem = Geo<PAIR, OUT_F32>::kSmem;
+    constexpr size_t smem = Geo<PAIR, OUT_F32 ? 0 : 2>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -509,38 +324,44 @@ cudaError_t dispatch(const GemmDesc& g, const CUtensorMap& ma, const CUtensorMap
     return launch_one<false, false, true, PAIR>(ma, mb, md, kp, grid, stream);
 }
 
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+bool make_tensor_map(void* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer,
+                     bool f32, std::string* why) {
+    return make_map(static_cast<CUtensorMap*>(map), base, inner, outer, ld, box_outer, why, f32);
+}
+
 // Choose the tile order that moves the fewest operand bytes from DRAM: keep
 // a group of one operand's blocks (at most kL2Budget bytes) resident in L2
 // and stream the other operand once per group.
-void choose_raster(const GemmDesc& g, int tile_m, KParams& kp) {
+void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int32_t* raster, int32_t* group) {
     constexpr double kL2Budget = 64.0 * 1024 * 1024;
-    const double a_blk = double(tile_m) * double(g.k_dim) * 2;
-    const double b_blk = double(kBlockN) * double(g.k_dim) * 2;
-    const double a_tot = a_blk * kp.num_m, b_tot = b_blk * kp.num_n;
-    const int gm = std::max(1, std::min(kp.num_m, int(kL2Budget / a_blk)));
-    const int gn = std::max(1, std::min(kp.num_n, int(kL2Budget / b_blk)));
-    const double t0 = a_tot + b_tot * double((kp.num_m + gm - 1) / gm);
-    const double t1 = b_tot + a_tot * double((kp.num_n + gn - 1) / gn);
+    const double a_blk = double(tile_m) * double(k_dim) * 2;
+    const double b_blk = double(kBlockN) * double(k_dim) * 2;
+    const double a_tot = a_blk * num_m, b_tot = b_blk * num_n;
+    const int gm = std::max(1, std::min(num_m, int(kL2Budget / a_blk)));
+    const int gn = std::max(1, std::min(num_n, int(kL2Budget / b_blk)));
+    const double t0 = a_tot + b_tot * double((num_m + gm - 1) / gm);
+    const double t1 = b_tot + a_tot * double((num_n + gn - 1) / gn);
     if (t1 < t0) {
-        kp.raster = 1;
-        kp.group = gn;
+        *raster = 1;
+        *group = gn;
     } else {
-        kp.raster = 0;
-        kp.group = gm;
+        *raster = 0;
+        *group = gm;
     }
 }
 
-bool use_pair() {
+bool cta_pair_enabled() {
     static const bool pair = [] {
         const char* e = std::getenv("TILED_LINEAR_CTA_PAIR");
         return !(e && e[0] == '0');
     }();
     return pair;
 }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-}  // namespace
 
 std::string gemm_check(const GemmDesc& g) {
     if (g.m_dim < 1 || g.n_dim < 1 || g.k_dim < 1) return "GEMM sizes must be >= 1";
@@ -573,7 +394,7 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
         if (why) *why = bad;
         return cudaErrorInvalidValue;
     }
-    const bool pair = use_pair() && num_sms >= 2;
+    const bool pair = cta_pair_enabled() && num_sms >= 2;
     const int tile_m = pair ? 2 * kBlockM : kBlockM;
     const uint32_t b_rows = pair ? kBlockN / 2 : kBlockN;
     CUtensorMap ma, mb;
@@ -594,7 +415,7 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     kp.num_n = int32_t((g.n_dim + kBlockN - 1) / kBlockN);
     kp.num_k = int32_t((g.k_dim + kBlockK - 1) / kBlockK);
     kp.num_tiles = kp.num_m * kp.num_n;
-    choose_raster(g, tile_m, kp);
+    choose_tile_order(g.k_dim, tile_m, kp.num_m, kp.num_n, &kp.raster, &kp.group);
     kp.d = g.d;
     kp.ldd = g.ldd;
     kp.accumulate = g.accumulate ? 1 : 0;

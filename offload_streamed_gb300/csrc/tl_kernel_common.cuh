@@ -1,0 +1,258 @@
+// tl_kernel_common.cuh -- device building blocks shared by the per-tile GEMM
+// kernel (tl_gemm.cu) and the persistent streamed-pass kernel (tl_pass.cu):
+// tile geometry, bounded waits, tile order, shared-memory operand
+// descriptors, the two epilogue paths, and acquire / release flag helpers.
+#pragma once
+#include "tl_gemm.h"
+#include "tl_ptx.cuh"
+
+#include <cuda_bf16.h>
+
+namespace tl {
+namespace kc {
+
+constexpr int kUmmaK = 16;
+constexpr uint32_t kStageA = kBlockM * kBlockK * 2;  // 128 rows of A per CTA: 16 KiB
+constexpr uint32_t kMnChunk = 64 * kBlockK * 2;      // 64 MN elements x 64 K rows = 8 KiB
+constexpr uint32_t kTmemCols = 2 * kBlockN;          // two fp32 accumulators of 256 columns
+constexpr int kThreads = 256;
+constexpr int kFirstEpilogueWarp = 4;
+// Epilogue staging: each of the 4 epilogue warps owns boxes of 32 output rows
+// x 128 bytes (64 bf16 columns) for its TMA stores.
+constexpr uint32_t kEpiBuf = 32 * 128;
+constexpr uint32_t kBarBytes = 512;
+
+static_assert(kBlockK * 2 == 128, "one K-block row must be one 128-byte swizzle row");
+
+// Tile geometry.  Single CTA: 128 x 256 output tile, B = 256 rows of N per
+// stage.  CTA pair (cta_group::2): 256 x 256 output tile; each CTA loads its
+// own 128 rows of A and its own 128 rows (N) of B, and the pair's MMA reads
+// both CTAs' shared memory.  EPI_BOXES staging boxes per epilogue warp.
+template <bool PAIR, int EPI_BOXES>
+struct Geo {
+    static constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;
+    static constexpr int kBRows = PAIR ? kBlockN / 2 : kBlockN;
+    static constexpr uint32_t kStageB = uint32_t(kBRows) * kBlockK * 2;
+    static constexpr uint32_t kStageBytes = kStageA + kStageB;
+    static constexpr uint32_t kEpiBytes = 4u * EPI_BOXES * kEpiBuf;
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + kEpiBytes + kBarBytes + 1024;
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+struct WaitCtx {
+    int32_t* err;
+    uint64_t timeout_ns;
+};
+
+__device__ __noinline__ inline bool wait_slow(uint32_t bar, uint32_t parity, int32_t* err, int32_t code,
+                                              bool stop_on_error, uint64_t timeout_ns) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 255u) == 0) {
+            if (stop_on_error && *reinterpret_cast<volatile int32_t*>(err) != 0) return false;
+            if (global_timer_ns() - t0 > timeout_ns) {
+                atomicOr(err, code);
+                return false;
+            }
+        }
+    }
+}
+
+// The MMA thread's waits use the base limit; the producer's wait for a free
+// stage and the epilogue's wait for an accumulator (both downstream of the
+// MMA thread) use twice that, so when a pipeline stalls the role nearest the
+// stall reports first.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w, int32_t code,
+                                             bool stop_on_error = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const bool downstream = code == kErrProducerWait || code == kErrEpilogueWait;
+    return wait_slow(bar, parity, w.err, code, stop_on_error, downstream ? 2 * w.timeout_ns : w.timeout_ns);
+}
+
+// Warp-uniform wait: lane 0 waits (bounded); then every lane observes the
+// completed phase itself, which cannot move on before this warp arrives.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, int32_t code,
+                                          int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bounded(bar, parity, w, code) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) return false;
+    int mine = 0;
+    for (int n = 0; n < (1 << 20) && !mine; ++n) mine = mbar_try_wait(bar, parity) ? 1 : 0;
+    if (!mine) atomicOr(w.err, code);
+    return __all_sync(0xffffffffu, mine) != 0;
+}
+
+// Output tile order: groups of `group` blocks along one dimension, walking
+// the other dimension inside the group, so that the group's blocks of one
+// operand stay in L2 while the other operand streams past once per group.
+// raster 0: groups of m-blocks (m fastest); 1: groups of n-blocks.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int raster, int group, int& mb,
+                                            int& nb) {
+    const int outer = raster == 0 ? num_m : num_n;
+    const int inner = raster == 0 ? num_n : num_m;
+    const int group_tiles = group * inner;
+    const int g = tile / group_tiles;
+    const int first = g * group;
+    const int width = min(group, outer - first);
+    const int local = tile - g * group_tiles;
+    const int a = first + local % width;
+    const int b = local / width;
+    mb = raster == 0 ? a : b;
+    nb = raster == 0 ? b : a;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Shared-memory descriptor of UMMA_K step j (16 elements of K) of a stage
+// operand: K-major rows advance 32 bytes inside the 128-byte swizzle row,
+// MN-major operands advance 16 rows of 128 bytes.
+__device__ __forceinline__ uint64_t operand_desc(bool mn_major, uint32_t base, int j) {
+    return mn_major ? smem_desc_sw128(base + uint32_t(j) * 2048u, kMnChunk, 1024)
+                    : smem_desc_sw128(base + uint32_t(j) * 32u, 16, 1024);
+}
+
+// ---- epilogues ---------------------------------------------------------------
+// Warp q owns TMEM lanes 32q..32q+31 = output rows row0..row0+31 of the CTA's
+// half tile; lane l holds row row0 + l.  t_row addresses the warp's lanes of
+// the accumulator.
+
+// bf16: per 64-column chunk, two tcgen05.ld, pack, write the lane's 128-byte
+// row into a 128B-swizzled staging box (two per warp, alternating), and lane 0
+// issues a TMA store of the 32 x 64 box at (col0 + 64c, row0).
+__device__ __forceinline__ void epi_bf16_tma(const CUtensorMap* map, uint32_t t_row, uint32_t epi0, uint32_t& buf,
+                                             int nchunks, int col0, int row0, int lane) {
+    for (int c = 0; c < nchunks; ++c) {
+        uint32_t w[32];
+        uint32_t v[32];
+        tmem_ld_32cols(t_row + uint32_t(c) * 64u, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        tmem_ld_32cols(t_row + uint32_t(c) * 64u + 32u, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            w[16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        const uint32_t sbuf = epi0 + buf * kEpiBuf;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used sbuf has read it
+        __syncwarp();
+        const uint32_t row_addr = sbuf + uint32_t(lane) * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(row_addr + ((uint32_t(j) ^ (uint32_t(lane) & 7u)) << 4), w[4 * j], w[4 * j + 1],
+                         w[4 * j + 2], w[4 * j + 3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, sbuf, col0 + c * 64, row0);
+            bulk_commit_group();
+        }
+        buf ^= 1u;
+    }
+}
+
+// fp32: per 32-column chunk, tcgen05.ld and a direct 128-byte store of the
+// lane's row at out_row + 32c (columns past `rem0` are skipped); with `rmw`
+// the old values are added, the next chunk's loaded while this one is
+// added and stored.
+__device__ __forceinline__ void epi_f32_direct(float* out_row, bool row_ok, int rem0, uint32_t t_row, int nchunks,
+                                               bool rmw) {
+    auto load_old = [&](int c, float4(&dst)[8]) {
+        const float* src = out_row + c * 32;
+        const int rem = rem0 - c * 32;
+        if (row_ok && rem >= 32) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = reinterpret_cast<const float4*>(src)[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                dst[j].x = (row_ok && 4 * j + 0 < rem) ? src[4 * j + 0] : 0.f;
+                dst[j].y = (row_ok && 4 * j + 1 < rem) ? src[4 * j + 1] : 0.f;
+                dst[j].z = (row_ok && 4 * j + 2 < rem) ? src[4 * j + 2] : 0.f;
+                dst[j].w = (row_ok && 4 * j + 3 < rem) ? src[4 * j + 3] : 0.f;
+            }
+        }
+    };
+    float4 old[8];
+    if (rmw && nchunks > 0) load_old(0, old);
+    for (int c = 0; c < nchunks; ++c) {
+        uint32_t w[32];
+        tmem_ld_32cols(t_row + uint32_t(c) * 32u, w);
+        float4 nxt[8];
+        if (rmw && c + 1 < nchunks) load_old(c + 1, nxt);
+        tmem_ld_wait();
+        float4 val[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            val[j] = make_float4(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]),
+                                 __uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]));
+            if (rmw) {
+                val[j].x = old[j].x + val[j].x;
+                val[j].y = old[j].y + val[j].y;
+                val[j].z = old[j].z + val[j].z;
+                val[j].w = old[j].w + val[j].w;
+            }
+        }
+        float* dst = out_row + c * 32;
+        const int rem = rem0 - c * 32;
+        if (row_ok && rem >= 32) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) reinterpret_cast<float4*>(dst)[j] = val[j];
+        } else if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (4 * j + 0 < rem) dst[4 * j + 0] = val[j].x;
+                if (4 * j + 1 < rem) dst[4 * j + 1] = val[j].y;
+                if (4 * j + 2 < rem) dst[4 * j + 2] = val[j].z;
+                if (4 * j + 3 < rem) dst[4 * j + 3] = val[j].w;
+            }
+        }
+        if (rmw && c + 1 < nchunks) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) old[j] = nxt[j];
+        }
+    }
+}
+
+// ---- flags in global memory ----------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Order this thread's earlier generic-proxy accesses (e.g. a flag it read)
+// before its later async-proxy (TMA) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait (bounded by limit_ns) until the 32-bit sequence value at p has reached
+// `target` (wrap-safe: (int32)(value - target) >= 0).  One thread.
+__device__ __noinline__ inline bool poll_geq(const uint32_t* p, uint32_t target, const WaitCtx& w, int32_t code,
+                                             uint64_t limit_ns) {
+    if (int32_t(ld_acquire_u32(p) - target) >= 0) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        __nanosleep(200);
+        if (int32_t(ld_acquire_u32(p) - target) >= 0) return true;
+        if ((n & 63u) == 0) {
+            if (*reinterpret_cast<volatile int32_t*>(w.err) != 0) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                atomicOr(w.err, code);
+                return false;
+            }
+        }
+    }
+}
+
+}  // namespace kc
+}  // namespace tl

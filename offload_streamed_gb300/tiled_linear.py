@@ -43,6 +43,7 @@ class tl_stats(ctypes.Structure):
         ("sum_fwd_h2d_ms", ctypes.c_double), ("sum_bwd_total_ms", ctypes.c_double),
         ("sum_bwd_dw_gemm_ms", ctypes.c_double), ("sum_bwd_dx_gemm_ms", ctypes.c_double),
         ("sum_bwd_h2d_ms", ctypes.c_double), ("sum_bwd_d2h_ms", ctypes.c_double),
+        ("sum_bwd_gemm_ms", ctypes.c_double), ("bwd_gemm_ms", ctypes.c_float), ("persistent", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

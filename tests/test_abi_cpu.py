@@ -10,7 +10,8 @@ import pytest
 from oracle import closed_forms as CF
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "tiled_linear.h")
+HEADER_FILE = os.path.join(ROOT, "include", "tiled_linear.h")
+HEADER = 65536  # workspace control block: error word, pass flags and counters
 
 
 @pytest.fixture(scope="module")
@@ -23,7 +24,7 @@ def tl():
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = open(HEADER_FILE).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(tiled_linear_\w+)\s*\(", src)))
 
@@ -59,13 +60,13 @@ def test_workspace_bytes_matches_closed_form(tl, K, M, N, d):
     tile_al = (tile + 255) // 256 * 256
     ring = CF.ring_bytes(K, M, N, d) // tile * tile_al
     staging = min(2, N) * tile_al
-    assert tl.tiled_linear_workspace_bytes(K, M, N, d) == 4096 + ring + staging
+    assert tl.tiled_linear_workspace_bytes(K, M, N, d) == HEADER + ring + staging
 
 
 def test_workspace_bytes_auto_depth(tl):
     tile = CF.tile_bytes(1024, 4096, 4)
-    assert tl.tiled_linear_workspace_bytes(1024, 4096, 4, -1) == 4096 + (4 + 2) * tile
-    assert tl.tiled_linear_workspace_bytes(1024, 4096 * 4, 16, -1) == 4096 + (4 + 2) * tile
+    assert tl.tiled_linear_workspace_bytes(1024, 4096, 4, -1) == HEADER + (4 + 2) * tile
+    assert tl.tiled_linear_workspace_bytes(1024, 4096 * 4, 16, -1) == HEADER + (4 + 2) * tile
 
 
 @pytest.mark.parametrize("K,M,N,d", [(0, 64, 1, 0), (12, 64, 1, 0), (64, 65, 1, 0), (64, 64, 3, 0),

@@ -23,7 +23,21 @@ class Run:
     pass
 
 
-def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, stream=None):
+def make_op(tl, K, M, N, d, w, dw, tile_major=True, persistent=True):
+    """Create a handle; persistent=False forces one launch per tile and GEMM."""
+    import os
+    old = os.environ.get("TILED_LINEAR_PERSISTENT")
+    os.environ["TILED_LINEAR_PERSISTENT"] = "1" if persistent else "0"
+    try:
+        return tl.TiledLinear(K, M, N, d, w, dw, tile_major=tile_major)
+    finally:
+        if old is None:
+            del os.environ["TILED_LINEAR_PERSISTENT"]
+        else:
+            os.environ["TILED_LINEAR_PERSISTENT"] = old
+
+
+def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, stream=None, persistent=True):
     r = Run()
     w = tl.PinnedBuffer(K * M)
     dw = tl.PinnedBuffer(K * M)
@@ -31,7 +45,7 @@ def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, s
     dw.tensor.view(torch.int16).fill_(0x7FC0)  # NaN: catches tiles never written
     x = I.make_x(T, K, seed, kind=kind)
     dy = I.make_dy(T, M, seed, kind=kind)
-    op = tl.TiledLinear(K, M, N, d, w, dw, tile_major=tile_major)
+    op = make_op(tl, K, M, N, d, w, dw, tile_major=tile_major, persistent=persistent)
     xd, dyd = x.cuda(), dy.cuda()
     s = stream or torch.cuda.current_stream()
     with torch.cuda.stream(s):
@@ -62,14 +76,19 @@ def oracle_check(r, T, K, M):
     check("dW", r.dw.float().numpy(), dW, xa.T @ dya, T, True)
 
 
+@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "per_tile"])
 @pytest.mark.parametrize("tile_major", [True, False], ids=["tilemajor", "rowmajor"])
-def test_tiny_config_full_parity(tl, tile_major):
+def test_tiny_config_full_parity(tl, tile_major, persistent):
     """X [256,1024], W [1024,4096] in N=4 tiles, dY [256,4096], d=1."""
     T, K, M, N, d = 256, 1024, 4096, 4, 1
-    r = run_op(tl, T, K, M, N, d, tile_major=tile_major)
+    r = run_op(tl, T, K, M, N, d, tile_major=tile_major, persistent=persistent)
     oracle_check(r, T, K, M)
     st = r.stats
-    assert st["fwd_launches"] == N and st["bwd_launches"] == 2 * N
+    assert st["persistent"] == int(persistent)
+    if persistent:
+        assert st["fwd_launches"] == 1 and st["bwd_launches"] == 1
+    else:
+        assert st["fwd_launches"] == N and st["bwd_launches"] == 2 * N
     assert st["fwd_h2d_bytes"] == K * M * 2 and st["bwd_h2d_bytes"] == K * M * 2
     assert st["bwd_d2h_bytes"] == K * M * 2
     assert st["depth"] == d
@@ -93,18 +112,39 @@ def _same(a, b):
                        b.contiguous().view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
 
 
+def dx_group(persistent, d, N):
+    """Tiles per dX accumulation group: a persistent backward accumulates dX
+    over two tiles whenever the ring holds two (d >= 1); one launch per tile
+    accumulates one tile at a time."""
+    return 2 if (persistent and d != 0 and N >= 2) else 1
+
+
 def test_schedule_does_not_change_results(tl):
-    """Depth, host layout and repeated calls change only the schedule: all
-    outputs are bit-identical."""
+    """Depth, host layout, repeated calls and the launch mode change only the
+    schedule: Y and dW are bit-identical for every schedule; dX (an fp32 sum
+    whose grouping is part of the schedule) is bit-identical among schedules
+    with the same dX grouping and matches the oracle for every one."""
     T, K, M, N = 200, 264, 2048, 8
-    base = run_op(tl, T, K, M, N, 1, tile_major=True, seed=7)
-    oracle_check(base, T, K, M)
-    for d, tm, calls in [(0, True, 1), (2, True, 1), (3, False, 1), (7, True, 2), (12, False, 1),
-                         (-1, True, 3)]:
-        r = run_op(tl, T, K, M, N, d, tile_major=tm, seed=7, calls=calls)
-        assert _same(r.y, base.y), (d, tm)
-        assert _same(r.dx, base.dx), (d, tm)
-        assert _same(r.dw, base.dw), (d, tm)
+    base = {1: run_op(tl, T, K, M, N, 1, tile_major=True, seed=7, persistent=False),
+            2: run_op(tl, T, K, M, N, 1, tile_major=True, seed=7)}
+    for r in base.values():
+        oracle_check(r, T, K, M)
+    for d, tm, calls, pers in [(0, True, 1, True), (2, True, 1, True), (3, False, 1, True), (7, True, 2, True),
+                               (12, False, 1, True), (-1, True, 3, True), (1, True, 1, False),
+                               (0, False, 2, False), (5, True, 1, False), (-1, True, 2, False)]:
+        r = run_op(tl, T, K, M, N, d, tile_major=tm, seed=7, calls=calls, persistent=pers)
+        ref = base[dx_group(pers, d, N)]
+        assert _same(r.y, ref.y), (d, tm, pers)
+        assert _same(r.dw, ref.dw), (d, tm, pers)
+        assert _same(r.dx, ref.dx), (d, tm, pers)
+
+
+def test_dx_grouping_matches_oracle_for_odd_tile_counts(tl):
+    """N odd: the last dX group holds a single tile."""
+    T, K, M = 160, 512, 5 * 512
+    for d in (1, 2, 4):
+        r = run_op(tl, T, K, M, 5, d, seed=13)
+        oracle_check(r, T, K, M)
 
 
 def test_tiled_forward_bit_exact_vs_untiled(tl):
@@ -149,6 +189,15 @@ def test_ragged_token_counts(tl, T):
     oracle_check(r, T, K, M)
 
 
+@pytest.mark.parametrize("K,M,N", [(264, 1200, 3), (520, 776, 1)])
+def test_ragged_tile_width_runs_per_tile(tl, K, M, N):
+    """Tile widths that are not a multiple of 256 run one launch per tile."""
+    T = 150
+    r = run_op(tl, T, K, M, N, 1, seed=K)
+    assert r.stats["persistent"] == 0
+    oracle_check(r, T, K, M)
+
+
 def test_zero_tokens(tl):
     """T = 0: forward does nothing; backward writes dW = 0 (an empty sum)."""
     K, M, N = 64, 512, 2
@@ -176,17 +225,22 @@ def test_side_stream_and_default_stream(tl):
     assert _same(a.y, b.y) and _same(a.dx, b.dx) and _same(a.dw, b.dw)
 
 
-def test_stats_are_consistent(tl):
+@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "per_tile"])
+def test_stats_are_consistent(tl, persistent):
     T, K, M, N = 512, 1024, 8192, 8
-    r = run_op(tl, T, K, M, N, 2, seed=1, calls=2)
+    r = run_op(tl, T, K, M, N, 2, seed=1, calls=2, persistent=persistent)
     st = r.stats
     assert st["fwd_valid"] == 1 and st["bwd_valid"] == 1
     assert st["n_tiles"] == N and st["depth"] == 2
-    for k in ("fwd_total_ms", "fwd_gemm_ms", "fwd_h2d_ms", "bwd_total_ms", "bwd_dw_gemm_ms",
-              "bwd_dx_gemm_ms", "bwd_h2d_ms", "bwd_d2h_ms"):
+    assert st["fwd_calls"] == 2 and st["bwd_calls"] == 2
+    for k in ("fwd_total_ms", "fwd_gemm_ms", "fwd_h2d_ms", "bwd_total_ms", "bwd_gemm_ms", "bwd_h2d_ms",
+              "bwd_d2h_ms"):
         assert st[k] > 0, k
+    if not persistent:
+        assert st["bwd_dw_gemm_ms"] > 0 and st["bwd_dx_gemm_ms"] > 0
+        assert abs(st["bwd_dw_gemm_ms"] + st["bwd_dx_gemm_ms"] - st["bwd_gemm_ms"]) < 1e-3
     assert st["fwd_gemm_ms"] <= st["fwd_total_ms"] + 1e-3
-    assert st["bwd_dw_gemm_ms"] + st["bwd_dx_gemm_ms"] <= st["bwd_total_ms"] + 1e-3
+    assert st["bwd_gemm_ms"] <= st["bwd_total_ms"] + 1e-3
 
 
 def test_auto_depth_picks_within_ring(tl):
