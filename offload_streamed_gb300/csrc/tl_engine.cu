@@ -378,6 +378,11 @@ tl_status finish_auto_depth(tl_handle* h) {
 CUstream cu(cudaStream_t s) { return reinterpret_cast<CUstream>(s); }
 CUdeviceptr cuptr(const void* p) { return reinterpret_cast<CUdeviceptr>(p); }
 
+// dX is accumulated over pairs of tiles when the ring holds two tiles (d >= 1)
+// and the tile width splits into whole 64-deep K-blocks.  Both launch modes
+// use the same pairs, so their dX agree bit for bit.
+bool dx_pairs(const tl_handle* h) { return h->d >= 1 && h->s.N >= 2 && h->s.Mi % tl::kBlockK == 0; }
+
 tl::PassDesc pass_desc(const tl_handle* h, bool backward, int64_t T, uint64_t fetch_base, uint64_t stage_base) {
     tl::PassDesc d;
     d.backward = backward;
@@ -391,9 +396,7 @@ tl::PassDesc pass_desc(const tl_handle* h, bool backward, int64_t T, uint64_t fe
     for (int g = 0; g < d.nstage && g < tl::kMaxPassStages; ++g) d.stages[g] = h->stage[g];
     d.fetch_base = uint32_t(fetch_base);
     d.stage_base = uint32_t(stage_base);
-    // dX is accumulated over groups of two tiles (one dX read-modify-write
-    // per two tiles) whenever the ring holds two tiles.
-    d.dx_group = d.nslots >= 2 ? 2 : 1;
+    d.dx_group = dx_pairs(h) ? 2 : 1;
     d.flags = h->flags;
     d.done = h->done;
     d.dwdone = h->dwdone;
@@ -779,6 +782,12 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     if (!tp) return st;
     CallSlot& t = *tp;
     const int nslots = h->d + 1;
+    // dX is accumulated over pairs of tiles (i+1, i) -- one launch reducing
+    // over both, in ascending column order -- whenever the ring holds two
+    // tiles; a lone last tile (N odd) and d = 0 go one tile at a time.
+    const bool pairs = dx_pairs(h);
+    int pend_sl = -1;  // ring slot of the pair's first (higher) tile
+    int dx_launches = 0;
     TL_TRY(h, cudaEventRecord(t.start, cs));
     for (int j = 0; j < s.N; ++j) {
         const int i = s.N - 1 - j;
@@ -819,27 +828,42 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
         TL_TRY(h, cudaEventRecord(t.ev[7][j], h->d2h));
         TL_TRY(h, cudaEventRecord(h->ev_drained[gs], h->d2h));
 
-        // dX (+)= dY_i W_i^T, fp32; the first tile of the pass stores
+        if (pairs && pend_sl < 0 && j + 1 < s.N) {
+            // first tile of a pair: its dX is reduced with the next tile's
+            pend_sl = sl;
+            TL_TRY(h, cudaEventRecord(t.ev[2][j], cs));
+            TL_TRY(h, cudaEventRecord(t.ev[3][j], cs));
+            continue;
+        }
+        // dX (+)= dY_i W_i^T (+ dY_{i+1} W_{i+1}^T), fp32; the first launch stores
         TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
+        if (pend_sl >= 0) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[pend_sl], 0));
         TL_TRY(h, cudaEventRecord(t.ev[2][j], cs));
         tl::GemmDesc gx;
         gx.m_dim = T;
         gx.n_dim = s.K;
-        gx.k_dim = s.Mi;
+        gx.k_dim = pend_sl >= 0 ? 2 * s.Mi : s.Mi;
         gx.a = static_cast<const uint8_t*>(dy_dev) + size_t(i) * size_t(s.Mi) * 2;
         gx.lda = s.M;
         gx.a_mn_major = false;
         gx.b = h->slot[sl];
         gx.ldb = s.Mi;
         gx.b_mn_major = false;
+        if (pend_sl >= 0) {  // reduction rows Mi .. 2Mi-1 are tile i+1's
+            gx.b2 = h->slot[pend_sl];
+            gx.k_split = s.Mi;
+        }
         gx.d = dx_dev;
         gx.ldd = s.K;
         gx.out = tl::OutKind::F32;
-        gx.accumulate = (j > 0);
+        gx.accumulate = dx_launches > 0;
         gx.err = h->err_dev;
         if ((st = launch(h, gx, cs)) != TL_OK) return st;
+        ++dx_launches;
         TL_TRY(h, cudaEventRecord(t.ev[3][j], cs));
         TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
+        if (pend_sl >= 0) TL_TRY(h, cudaEventRecord(h->ev_free[pend_sl], cs));
+        pend_sl = -1;
     }
     // dW on the host is complete when `stream` is.
     for (int g = 0; g < h->nstage; ++g) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[g], 0));
@@ -847,7 +871,7 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
     t.nk = s.N;
     t.depth = h->d;
-    t.launches = 2 * s.N;
+    t.launches = s.N + dx_launches;
     t.h2d_bytes = int64_t(s.N) * int64_t(tb);
     t.d2h_bytes = int64_t(s.N) * int64_t(tb);
     end_call(h->bwd, t);

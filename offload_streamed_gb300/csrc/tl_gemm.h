@@ -27,6 +27,12 @@ struct GemmDesc {
     const void* b = nullptr;
     int64_t ldb = 0;
     bool b_mn_major = false;
+    // Optional second B segment (K-major B only): reduction rows k >= k_split
+    // are read from b2[n * ldb + (k - k_split)] instead of b.  k_split is a
+    // multiple of kBlockK with 0 < k_split < k_dim.  Lets one launch reduce
+    // over two weight tiles that sit in different ring slots.
+    const void* b2 = nullptr;
+    int64_t k_split = 0;
     void* d = nullptr;
     int64_t ldd = 0;
     OutKind out = OutKind::BF16;

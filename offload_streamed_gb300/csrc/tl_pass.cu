@@ -180,8 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1) pass_kernel(const __grid_constant
                 const int kpt = p.num_k[kind];                       // K-blocks per pass position
                 const int nk = kind == 0 ? kpt * b.gsz : kpt;        // a dX job spans its group
                 for (int kb = 0; kb < nk; ++kb, ++fills) {
-                    const int jj = b.j + (kind == 0 ? kb / kpt : 0);  // pass position of this K-block
-                    const int kbl = kind == 0 ? kb - (jj - b.j) * kpt : kb;
+                    // a dX job reduces its group's tiles in ascending tile
+                    // order (the group's last pass position first)
+                    const int seg = kind == 0 ? kb / kpt : 0;
+                    const int jj = b.j + (kind == 0 ? b.gsz - 1 - seg : 0);  // pass position of this K-block
+                    const int kbl = kb - seg * kpt;
                     const int i = BWD ? p.N - 1 - jj : jj;            // weight tile index
                     const uint32_t f = p.fetch_base + uint32_t(jj);
                     const int s = int(f % uint32_t(p.nslots));

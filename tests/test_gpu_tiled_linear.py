@@ -88,7 +88,8 @@ def test_tiny_config_full_parity(tl, tile_major, persistent):
     if persistent:
         assert st["fwd_launches"] == 1 and st["bwd_launches"] == 1
     else:
-        assert st["fwd_launches"] == N and st["bwd_launches"] == 2 * N
+        # one dW launch per tile, one dX launch per tile pair
+        assert st["fwd_launches"] == N and st["bwd_launches"] == N + (N + 1) // 2
     assert st["fwd_h2d_bytes"] == K * M * 2 and st["bwd_h2d_bytes"] == K * M * 2
     assert st["bwd_d2h_bytes"] == K * M * 2
     assert st["depth"] == d
@@ -112,11 +113,11 @@ def _same(a, b):
                        b.contiguous().view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
 
 
-def dx_group(persistent, d, N):
-    """Tiles per dX accumulation group: a persistent backward accumulates dX
-    over two tiles whenever the ring holds two (d >= 1); one launch per tile
-    accumulates one tile at a time."""
-    return 2 if (persistent and d != 0 and N >= 2) else 1
+def dx_group(d, N, Mi):
+    """Tiles per dX accumulation group: both launch modes reduce dX over pairs
+    of tiles whenever the ring holds two (d >= 1) and the tile width is a
+    multiple of 64; otherwise one tile at a time."""
+    return 2 if (d != 0 and N >= 2 and Mi % 64 == 0) else 1
 
 
 def test_schedule_does_not_change_results(tl):
@@ -125,25 +126,26 @@ def test_schedule_does_not_change_results(tl):
     whose grouping is part of the schedule) is bit-identical among schedules
     with the same dX grouping and matches the oracle for every one."""
     T, K, M, N = 200, 264, 2048, 8
-    base = {1: run_op(tl, T, K, M, N, 1, tile_major=True, seed=7, persistent=False),
-            2: run_op(tl, T, K, M, N, 1, tile_major=True, seed=7)}
+    base = {1: run_op(tl, T, K, M, N, 0, tile_major=True, seed=7, persistent=False),
+            2: run_op(tl, T, K, M, N, 1, tile_major=True, seed=7, persistent=False)}
     for r in base.values():
         oracle_check(r, T, K, M)
     for d, tm, calls, pers in [(0, True, 1, True), (2, True, 1, True), (3, False, 1, True), (7, True, 2, True),
                                (12, False, 1, True), (-1, True, 3, True), (1, True, 1, False),
                                (0, False, 2, False), (5, True, 1, False), (-1, True, 2, False)]:
         r = run_op(tl, T, K, M, N, d, tile_major=tm, seed=7, calls=calls, persistent=pers)
-        ref = base[dx_group(pers, d, N)]
+        ref = base[dx_group(d, N, M // N)]
         assert _same(r.y, ref.y), (d, tm, pers)
         assert _same(r.dw, ref.dw), (d, tm, pers)
         assert _same(r.dx, ref.dx), (d, tm, pers)
 
 
-def test_dx_grouping_matches_oracle_for_odd_tile_counts(tl):
+@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "per_tile"])
+def test_dx_grouping_matches_oracle_for_odd_tile_counts(tl, persistent):
     """N odd: the last dX group holds a single tile."""
     T, K, M = 160, 512, 5 * 512
     for d in (1, 2, 4):
-        r = run_op(tl, T, K, M, 5, d, seed=13)
+        r = run_op(tl, T, K, M, 5, d, seed=13, persistent=persistent)
         oracle_check(r, T, K, M)
 
 
@@ -189,9 +191,10 @@ def test_ragged_token_counts(tl, T):
     oracle_check(r, T, K, M)
 
 
-@pytest.mark.parametrize("K,M,N", [(264, 1200, 3), (520, 776, 1)])
+@pytest.mark.parametrize("K,M,N", [(264, 1200, 3), (520, 776, 1), (264, 960, 3)])
 def test_ragged_tile_width_runs_per_tile(tl, K, M, N):
-    """Tile widths that are not a multiple of 256 run one launch per tile."""
+    """Tile widths that are not a multiple of 256 run one launch per tile;
+    a width of 320 (five 64-deep K-blocks) still pairs the dX tiles."""
     T = 150
     r = run_op(tl, T, K, M, N, 1, seed=K)
     assert r.stats["persistent"] == 0
@@ -237,6 +240,7 @@ def test_stats_are_consistent(tl, persistent):
               "bwd_d2h_ms"):
         assert st[k] > 0, k
     if not persistent:
+        assert st["bwd_launches"] == N + N // 2
         assert st["bwd_dw_gemm_ms"] > 0 and st["bwd_dx_gemm_ms"] > 0
         assert abs(st["bwd_dw_gemm_ms"] + st["bwd_dx_gemm_ms"] - st["bwd_gemm_ms"]) < 1e-3
     assert st["fwd_gemm_ms"] <= st["fwd_total_ms"] + 1e-3
