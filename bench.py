@@ -401,6 +401,71 @@ def run_e2e(op, cfg, x, dy, steps: int, warmup: int):
     return ms, h2d, d2h
 
 
+# DRAM traffic per launch of each GEMM kernel, from an ncu capture of
+# `bench.py --profile-gemms 2` (profiles/dram_traffic_gpt_tile.txt).  The file
+# records a hash of the kernel sources it was taken with; once they change the
+# figure no longer describes the kernel and the bench reports null.
+KERNEL_SOURCES = ["tl_gemm.cu", "tl_gemm.h", "tl_kernel_common.cuh", "tl_ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_gpt_tile.txt")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "offload_streamed_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def load_traffic(config: str) -> dict:
+    """{kernel key: DRAM bytes per launch} if the profile matches the current
+    kernel sources and this workload, else {}."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            kv = dict(l.split(":", 1) for l in fh.read().splitlines() if ":" in l and not l.startswith("#"))
+    except OSError:
+        return {}
+    kv = {k.strip(): v.strip() for k, v in kv.items()}
+    if kv.get("source_sha256") != kernel_source_hash() or kv.get("config") != config:
+        return {}
+    return {k: int(v) for k, v in kv.items() if k.endswith("_bytes_per_launch")}
+
+
+def profile_gemms(cfg, reps: int) -> None:
+    """The three resident GEMMs of one tile (dX of one tile pair, as a step
+    runs it) of the workload, `reps` times in the order fwd, dW, dX: a small
+    fixed launch sequence for ncu captures of each kernel (inputs above L2,
+    under 1 GiB on the device)."""
+    import torch
+
+    import __graft_entry__ as g
+    from offload_streamed_gb300 import inputs as I
+    from offload_streamed_gb300 import tiled_linear as tl
+
+    g.build()
+    T, K, M, N = cfg["T"], cfg["K"], cfg["M"], cfg["N"]
+    Mi = M // N
+    nx = 2 * Mi if (cfg["d"] != 0 and N >= 2 and Mi % 64 == 0) else Mi
+    x = I.make_x(T, K, 0, device="cuda")
+    dy = I.make_dy(T, nx, 0, device="cuda")
+    w = I.make_w_tile(K, nx, 0, 0, device="cuda")   # a tile pair, row-major [K, nx]
+    w1 = w[:, :Mi].contiguous()                      # one tile, as a ring slot holds it
+    y = torch.empty(T, Mi, dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty(K, Mi, dtype=torch.bfloat16, device="cuda")
+    dx = torch.zeros(T, K, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    for _ in range(reps):
+        tl.tiled_linear_gemm_forward(T, K, Mi, x.data_ptr(), K, w1.data_ptr(), Mi, y.data_ptr(), Mi, err.data_ptr(), st)
+        tl.tiled_linear_gemm_dw(T, K, Mi, x.data_ptr(), K, dy.data_ptr(), nx, dw.data_ptr(), Mi, err.data_ptr(), st)
+        tl.tiled_linear_gemm_dx(T, K, nx, dy.data_ptr(), nx, w.data_ptr(), nx, dx.data_ptr(), K, 1, err.data_ptr(), st)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit(f"profile_gemms: kernel timeout word {int(err.item())}")
+    log(f"[bench] profile-gemms: {reps} x (fwd, dW, dX over {nx} columns) at T={T} K={K} Mi={Mi}")
+
+
 # ----------------------------------------------------------------------------
 def run_ours(args, cfg, dist: Dist):
     import torch
@@ -480,8 +545,25 @@ def run_ours(args, cfg, dist: Dist):
                 "peak_kind": f"bf16 dense sustained, {peaks['source']}",
                 "flops_per_launch": dom_flops, "avg_launch_ms": round(dom_ms, 4),
                 "traffic": None,
+                "algorithmic_bytes_per_launch": None,
                 "all_kernels_tflops": {k: round(f / (ms / 1e3) / 1e12, 1) for k, (ms, f) in kern.items()
                                        if ms > 0}}
+
+    if not persistent:
+        # algorithmic HBM bytes per launch (operands once, outputs once, the
+        # dX read-modify-write) and the ncu-measured DRAM bytes, if current
+        kind = dom.split(" ")[0]
+        nx = 2 * Mi if n_dx * 2 == N else Mi
+        algo = {"fwd_gemm": 2 * T * K + 2 * K * Mi + 2 * T * Mi,
+                "dw_gemm": 2 * T * K + 2 * T * Mi + 2 * K * Mi,
+                "dx_gemm": 2 * T * nx + 2 * K * nx + 8 * T * K}[kind]
+        roofline["algorithmic_bytes_per_launch"] = algo
+        traffic = load_traffic(args.config)
+        key = {"fwd_gemm": "fwd_gemm", "dw_gemm": "dw_gemm", "dx_gemm": "dx_gemm_pair"}[kind]
+        if nx == 2 * Mi or kind != "dx_gemm":
+            roofline["traffic"] = traffic.get(key + "_bytes_per_launch")
+        roofline["traffic_source"] = "profiles/dram_traffic_gpt_tile.txt (ncu dram__bytes_read.sum + " \
+                                     "dram__bytes_write.sum; null when the kernel sources changed since)"
 
     out = {"metric": METRIC, "value": None, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
@@ -599,6 +681,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--profile-gemms", type=int, default=0, metavar="R",
+                    help="only run the three resident GEMMs of one tile R times (for ncu), print nothing")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         log("[bench] note: fewer than 3 warm-up steps")
@@ -608,6 +692,9 @@ def main():
     if args.T is not None:
         cfg["T"] = args.T
         cfg["workload"] += f" (T overridden to {args.T})"
+    if args.profile_gemms > 0:
+        profile_gemms(cfg, args.profile_gemms)
+        return
     if args.impl == "reference":
         # rank 0 alone times the CPU oracle; other ranks have nothing to do
         if int(os.environ.get("RANK", "0")) != 0:

@@ -347,9 +347,13 @@ bool make_tensor_map(void* map, const void* base, uint64_t inner, uint64_t outer
 
 // Choose the tile order that moves the fewest operand bytes from DRAM: keep
 // a group of one operand's blocks (at most kL2Budget bytes) resident in L2
-// and stream the other operand once per group.
+// and stream the other operand once per group.  The budget is a quarter of
+// the L2: the persistent CTAs drift apart in K, so a group's blocks must
+// share the cache with the streamed operand's slices in flight (32 MiB
+// measured best or equal for all three GEMMs at the GPT-scale tile, against
+// 16, 48, 64 and 128 MiB, under the power cap).
 void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int32_t* raster, int32_t* group) {
-    constexpr double kL2Budget = 64.0 * 1024 * 1024;
+    constexpr double kL2Budget = 32.0 * 1024 * 1024;
     const double a_blk = double(tile_m) * double(k_dim) * 2;
     const double b_blk = double(kBlockN) * double(k_dim) * 2;
     const double a_tot = a_blk * num_m, b_tot = b_blk * num_n;
