@@ -619,6 +619,34 @@ def run_ours(args, cfg, dist: Dist):
                       "what": "X, dY copied from pinned host memory and Y, dX read back every step "
                               "(weights streamed as always)"}
 
+    # --- tile reuse (an extension, reported apart from the method's metric) --
+    # The backward takes the min(d+1, N) tiles the forward left in the ring
+    # instead of fetching them again (tiled_linear_set_tile_reuse).
+    if not args.skip_aux and not persistent:
+        op.set_tile_reuse(True)
+        for _ in range(3):
+            op.forward(x, y, stream=s)
+            op.backward(x, dy, dx, stream=s)
+        torch.cuda.synchronize()
+        op.reset_stats()
+        k = max(3, min(args.steps, 30))
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(s)
+        for _ in range(k):
+            op.forward(x, y, stream=s)
+            op.backward(x, dy, dx, stream=s)
+        r1.record(s)
+        torch.cuda.synchronize()
+        r_ms = dist.max(r0.elapsed_time(r1) / k)
+        rs = op.stats()
+        op.set_tile_reuse(False)
+        out["tile_reuse"] = {
+            "value": round(dist.world * flops_step / (r_ms / 1e3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(r_ms, 4), "steps": k, "bwd_reused_tiles": rs["bwd_reused_tiles"],
+            "h2d_bytes_per_step": rs["fwd_h2d_bytes"] + rs["bwd_h2d_bytes"],
+            "what": "backward reuses the tiles still resident from forward (not the pages' method, which "
+                    "refetches every tile; W unchanged between the two calls)"}
+
     # --- CPU oracle baseline ----------------------------------------------------
     if want_cpu:
         xh, dyh = x.cpu(), dy.cpu()

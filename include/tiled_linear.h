@@ -88,6 +88,8 @@ typedef struct {
     double sum_bwd_gemm_ms;
     float bwd_gemm_ms;
     int32_t persistent;
+    int32_t bwd_reused_tiles; /* tiles the last backward took from the ring
+                                 instead of fetching (tiled_linear_set_tile_reuse) */
 } tl_stats;
 
 /* Device workspace bytes needed for (K, M, N, d): (min(d,N-1)+1) weight slots
@@ -167,6 +169,21 @@ tl_status tiled_linear_get_stats(tl_handle *h, void *tl_stats_out);
 
 /* Wait for every recorded call to finish and zero the sum_* counters. */
 tl_status tiled_linear_reset_stats(tl_handle *h);
+
+/* Tile reuse across calls -- an opt-in extension; the method itself fetches
+ * every tile again for the backward (tm_zero_infinity, "The FLOPs-per-byte
+ * test": parameters climb the hierarchy twice per step).  The prefetcher
+ * follows the operator sequence: it knows which tiles come next
+ * (pwwt.cn/news/5430303, 关键技术三 (1) 动态预取器).  With enable != 0, a
+ * backward call takes the tiles its descending order starts with from the
+ * ring when the calls before it left them there -- after a forward, the last
+ * min(d+1, N) tiles -- instead of fetching them again.  tl_stats reports them
+ * as bwd_reused_tiles, and bwd_h2d_bytes drops by as many tiles.  Results are
+ * bit-identical to refetching as long as the host W buffer is not written
+ * between the calls; writing it there is undefined.  Default: off.  Errors:
+ * TL_ERR_INVALID in the persistent launch mode, TL_ERR_STATE on a failed
+ * handle. */
+tl_status tiled_linear_set_tile_reuse(tl_handle *h, int32_t enable);
 
 /* --- resident GEMMs: the three kernels on device-resident operands --------
  * The same kernels the engine launches per tile, for callers that already

@@ -31,6 +31,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <deque>
 #include <mutex>
 #include <new>
 #include <string>
@@ -114,7 +115,7 @@ struct CallSlot {
     bool pending = false;  // recorded, not yet harvested
     bool harvested = false;
     int32_t nk = 0;        // kernel spans recorded (N per-tile launches, or 1 pass)
-    int32_t depth = 0, launches = 0;
+    int32_t depth = 0, launches = 0, reused = 0;
     int64_t h2d_bytes = 0, d2h_bytes = 0;
     float total = 0, gemm1 = 0, gemm2 = 0, h2d = 0, d2h = 0;
 };
@@ -149,6 +150,13 @@ struct tl_handle {
     cudaStream_t h2d = nullptr, d2h = nullptr;
     std::vector<cudaEvent_t> ev_ready, ev_free, ev_dwdone, ev_drained;
     uint64_t fetch_seq = 0, stage_seq = 0;
+    // One launch per tile: the ring slots in the order their last readers
+    // were enqueued (a fetch takes the front: the slot freed earliest), the
+    // tile each slot holds (-1: none), and whether a backward takes the
+    // tiles it starts with from the ring when they are still there.
+    std::deque<int> slot_q;
+    std::vector<int32_t> slot_tile;
+    bool reuse = false;
     int num_sms = 0;
     bool persistent = false;  // whole passes as one persistent launch
     uint32_t* flags = nullptr;
@@ -341,6 +349,22 @@ void end_call(Phase& p, CallSlot& c) {
     p.calls += 1;
 }
 
+// One launch per tile: slots 0..d free in order, holding no tile.
+void reset_ring(tl_handle* h) {
+    h->slot_q.clear();
+    for (int s = 0; s <= h->d; ++s) h->slot_q.push_back(s);
+    h->slot_tile.assign(size_t(h->slot_cap), -1);
+}
+
+// The slot for the next fetch: the one whose last reader was enqueued
+// earliest (the fetch waits for that reader on the h2d stream).
+int take_slot(tl_handle* h) {
+    if (h->slot_q.empty()) return -1;
+    const int sl = h->slot_q.front();
+    h->slot_q.pop_front();
+    return sl;
+}
+
 // Automatic depth: after the first forward call, d = ceil(t_fetch / t_layer)
 // from that call's measured copy and kernel spans (tm_zero_infinity,
 // "Prefetch depth"), bounded by the slots the workspace holds.
@@ -369,6 +393,7 @@ tl_status finish_auto_depth(tl_handle* h) {
             h->fetch_seq = 0;
         }
         h->d = dnew;
+        reset_ring(h);
     }
     h->auto_pending = false;
     return TL_OK;
@@ -512,6 +537,7 @@ tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t 
     h->dxdone = reinterpret_cast<uint32_t*>(h->ws + kDxDoneOffset);
     uint8_t* p = h->ws + kHeaderBytes;
     for (int s = 0; s < h->slot_cap; ++s, p += tb) h->slot.push_back(p);
+    reset_ring(h);
     for (int g = 0; g < h->nstage; ++g, p += tb) h->stage.push_back(p);
 
     if (cudaMemset(h->ws, 0, kHeaderBytes) != cudaSuccess ||
@@ -711,13 +737,15 @@ tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void*
     CallSlot* tp = begin_call(h, h->fwd, &st);
     if (!tp) return st;
     CallSlot& t = *tp;
-    const int nslots = h->d + 1;
     TL_TRY(h, cudaEventRecord(t.start, cs));
     for (int i = 0; i < s.N; ++i) {
-        const int sl = int(h->fetch_seq++ % uint64_t(nslots));
+        const int sl = take_slot(h);
+        if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
+        h->slot_tile[size_t(sl)] = -1;
         TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
         TL_TRY(h, cudaEventRecord(t.ev[4][i], h->h2d));
         TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
+        h->slot_tile[size_t(sl)] = i;
         TL_TRY(h, cudaEventRecord(t.ev[5][i], h->h2d));
         TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
 
@@ -740,6 +768,7 @@ tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void*
         if ((st = launch(h, g, cs)) != TL_OK) return st;
         TL_TRY(h, cudaEventRecord(t.ev[1][i], cs));
         TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
+        h->slot_q.push_back(sl);
     }
     TL_TRY(h, cudaEventRecord(t.end, cs));
     TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
@@ -781,7 +810,23 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     CallSlot* tp = begin_call(h, h->bwd, &st);
     if (!tp) return st;
     CallSlot& t = *tp;
-    const int nslots = h->d + 1;
+    // With reuse on, the longest prefix of the descending tile order that is
+    // still resident in the ring (the last d+1 tiles a forward fetched) is
+    // taken as it is; those slots leave the free queue until their dX launch.
+    std::vector<int> resident(size_t(s.N), -1);
+    int reused = 0;
+    if (h->reuse) {
+        for (int sl = 0; sl <= h->d; ++sl)
+            if (h->slot_tile[size_t(sl)] >= 0) resident[size_t(h->slot_tile[size_t(sl)])] = sl;
+        while (reused < s.N && resident[size_t(s.N - 1 - reused)] >= 0) ++reused;
+        std::deque<int> q;
+        for (int sl : h->slot_q) {
+            bool taken = false;
+            for (int j = 0; j < reused; ++j) taken = taken || resident[size_t(s.N - 1 - j)] == sl;
+            if (!taken) q.push_back(sl);
+        }
+        h->slot_q.swap(q);
+    }
     // dX is accumulated over pairs of tiles (i+1, i) -- one launch reducing
     // over both, in ascending column order -- whenever the ring holds two
     // tiles; a lone last tile (N odd) and d = 0 go one tile at a time.
@@ -791,14 +836,23 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     TL_TRY(h, cudaEventRecord(t.start, cs));
     for (int j = 0; j < s.N; ++j) {
         const int i = s.N - 1 - j;
-        const int sl = int(h->fetch_seq++ % uint64_t(nslots));
         const int gs = int(h->stage_seq++ % uint64_t(h->nstage));
-        // refetch W_i
-        TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
-        TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
-        TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
-        TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
-        TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
+        int sl;
+        if (j < reused) {  // W_i is still in the ring
+            sl = resident[size_t(i)];
+            TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
+            TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
+        } else {  // refetch W_i
+            sl = take_slot(h);
+            if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
+            h->slot_tile[size_t(sl)] = -1;
+            TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
+            TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
+            TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
+            TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
+            TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
+            h->slot_tile[size_t(sl)] = i;
+        }
 
         // dW_i = X^T dY_i into staging slot gs (does not need W_i)
         TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gs], 0));
@@ -862,7 +916,11 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
         ++dx_launches;
         TL_TRY(h, cudaEventRecord(t.ev[3][j], cs));
         TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
-        if (pend_sl >= 0) TL_TRY(h, cudaEventRecord(h->ev_free[pend_sl], cs));
+        if (pend_sl >= 0) {
+            TL_TRY(h, cudaEventRecord(h->ev_free[pend_sl], cs));
+            h->slot_q.push_back(pend_sl);
+        }
+        h->slot_q.push_back(sl);
         pend_sl = -1;
     }
     // dW on the host is complete when `stream` is.
@@ -872,7 +930,8 @@ tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, cons
     t.nk = s.N;
     t.depth = h->d;
     t.launches = s.N + dx_launches;
-    t.h2d_bytes = int64_t(s.N) * int64_t(tb);
+    t.reused = reused;
+    t.h2d_bytes = int64_t(s.N - reused) * int64_t(tb);
     t.d2h_bytes = int64_t(s.N) * int64_t(tb);
     end_call(h->bwd, t);
     return TL_OK;
@@ -947,6 +1006,7 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
         out->bwd_h2d_bytes = c.h2d_bytes;
         out->bwd_d2h_bytes = c.d2h_bytes;
         out->bwd_launches = c.launches;
+        out->bwd_reused_tiles = c.reused;
     }
     out->fwd_calls = h->fwd.sum_calls;
     out->sum_fwd_total_ms = h->fwd.sum_total;
@@ -966,6 +1026,15 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
         return fail(h, TL_ERR_TIMEOUT,
                     "a kernel's bounded wait timed out (error bits " + std::to_string(word) + ")");
     return h->sticky;
+}
+
+tl_status tiled_linear_set_tile_reuse(tl_handle* h, int32_t enable) {
+    tl_status st = check_usable(h);
+    if (st != TL_OK) return st;
+    if (enable && h->persistent)
+        return fail(h, TL_ERR_INVALID, "tile reuse needs the per-tile launch mode (TILED_LINEAR_PERSISTENT=1 is set)");
+    h->reuse = enable != 0;
+    return TL_OK;
 }
 
 tl_status tiled_linear_reset_stats(tl_handle* h) {

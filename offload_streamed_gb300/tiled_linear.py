@@ -44,6 +44,7 @@ class tl_stats(ctypes.Structure):
         ("sum_bwd_dw_gemm_ms", ctypes.c_double), ("sum_bwd_dx_gemm_ms", ctypes.c_double),
         ("sum_bwd_h2d_ms", ctypes.c_double), ("sum_bwd_d2h_ms", ctypes.c_double),
         ("sum_bwd_gemm_ms", ctypes.c_double), ("bwd_gemm_ms", ctypes.c_float), ("persistent", ctypes.c_int32),
+        ("bwd_reused_tiles", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -89,6 +90,8 @@ def load():
         L.tiled_linear_get_stats.restype = st
         L.tiled_linear_reset_stats.argtypes = [vp]
         L.tiled_linear_reset_stats.restype = st
+        L.tiled_linear_set_tile_reuse.argtypes = [vp, i32]
+        L.tiled_linear_set_tile_reuse.restype = st
         L.tiled_linear_gemm_forward.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp]
         L.tiled_linear_gemm_forward.restype = st
         L.tiled_linear_gemm_dw.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp]
@@ -161,6 +164,10 @@ def tiled_linear_get_stats(h: int) -> dict:
 
 def tiled_linear_reset_stats(h: int) -> None:
     _check(load().tiled_linear_reset_stats(h), "tiled_linear_reset_stats", h)
+
+
+def tiled_linear_set_tile_reuse(h: int, enable: bool) -> None:
+    _check(load().tiled_linear_set_tile_reuse(h, 1 if enable else 0), "tiled_linear_set_tile_reuse", h)
 
 
 def tiled_linear_gemm_forward(T, K, n, x, ldx, w, ldw, y, ldy, err, stream) -> None:
@@ -293,6 +300,11 @@ class TiledLinear:
 
     def reset_stats(self) -> None:
         tiled_linear_reset_stats(self.handle)
+
+    def set_tile_reuse(self, enable: bool = True) -> None:
+        """Let backward calls take the tiles still resident from the calls
+        before them (W must not change in between)."""
+        tiled_linear_set_tile_reuse(self.handle, enable)
 
     def close(self) -> int:
         st = TL_OK

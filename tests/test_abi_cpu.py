@@ -109,3 +109,27 @@ def test_resident_gemm_argument_checks(tl):
     assert lib.tiled_linear_gemm_dw(64, 64, 64, 256, 60, 256, 64, 256, 64, 256, None) == tl.TL_ERR_INVALID
     assert lib.tiled_linear_gemm_dx(64, 64, 64, 256, 64, 256, 64, 256, 32, 0, 256, None) == tl.TL_ERR_INVALID
     assert lib.tiled_linear_gemm_dx(64, 64, 64, 258, 64, 256, 64, 256, 64, 0, 256, None) == tl.TL_ERR_INVALID
+
+
+def test_null_handle_tile_reuse(tl):
+    assert tl.load().tiled_linear_set_tile_reuse(None, 1) == tl.TL_ERR_STATE
+
+
+def test_stats_struct_layout_matches_the_header(tl, tmp_path):
+    """The binding's tl_stats mirrors the C struct field by field: a C program
+    built against include/tiled_linear.h prints sizeof and every offsetof."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc missing")
+    fields = [name for name, _ in tl.tl_stats._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"tiled_linear.h\"\nint main(void) {\n"
+                   "  printf(\"%zu\\n\", sizeof(tl_stats));\n"
+                   + "".join(f"  printf(\"%zu\\n\", offsetof(tl_stats, {f}));\n" for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(tl.tl_stats)
+    assert out[1:] == [getattr(tl.tl_stats, f).offset for f in fields]

@@ -37,7 +37,8 @@ def make_op(tl, K, M, N, d, w, dw, tile_major=True, persistent=True):
             os.environ["TILED_LINEAR_PERSISTENT"] = old
 
 
-def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, stream=None, persistent=True):
+def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, stream=None, persistent=True,
+           reuse=False, extra_backward=False):
     r = Run()
     w = tl.PinnedBuffer(K * M)
     dw = tl.PinnedBuffer(K * M)
@@ -46,6 +47,8 @@ def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, s
     x = I.make_x(T, K, seed, kind=kind)
     dy = I.make_dy(T, M, seed, kind=kind)
     op = make_op(tl, K, M, N, d, w, dw, tile_major=tile_major, persistent=persistent)
+    if reuse:
+        op.set_tile_reuse(True)
     xd, dyd = x.cuda(), dy.cuda()
     s = stream or torch.cuda.current_stream()
     with torch.cuda.stream(s):
@@ -54,6 +57,9 @@ def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, s
             dx = torch.full((T, K), float("nan"), dtype=torch.float32, device="cuda")
             op.forward(xd, y, stream=s)
             op.backward(xd, dyd, dx, stream=s)
+            if extra_backward:  # a second backward with no forward between
+                dx.fill_(float("nan"))
+                op.backward(xd, dyd, dx, stream=s)
     s.synchronize()
     r.stats = op.stats()
     r.y = y.cpu()
@@ -276,3 +282,44 @@ def test_host_workspace_is_rejected(tl):
     assert ei.value.status == tl.TL_ERR_WORKSPACE
     for b in (w, dw, ws):
         b.close()
+
+
+@pytest.mark.parametrize("N,d,calls", [(8, 2, 2), (5, 1, 2), (4, 0, 2), (3, 7, 1), (6, 3, 3), (8, -1, 3)])
+def test_tile_reuse_is_bit_identical_and_skips_fetches(tl, N, d, calls):
+    """With tile reuse on, the backward takes the last min(d+1, N) tiles from
+    the ring instead of fetching them again: same bits, fewer H2D bytes."""
+    T, K, Mi = 192, 512, 512
+    M = N * Mi
+    ref = run_op(tl, T, K, M, N, d, seed=21, calls=calls, persistent=False)
+    r = run_op(tl, T, K, M, N, d, seed=21, calls=calls, persistent=False, reuse=True)
+    assert _same(r.y, ref.y) and _same(r.dw, ref.dw) and _same(r.dx, ref.dx)
+    oracle_check(r, T, K, M)
+    want = min(r.stats["depth"] + 1, N)
+    assert r.stats["bwd_reused_tiles"] == want
+    assert r.stats["bwd_h2d_bytes"] == (N - want) * K * Mi * 2
+    assert ref.stats["bwd_reused_tiles"] == 0 and ref.stats["bwd_h2d_bytes"] == N * K * Mi * 2
+
+
+def test_tile_reuse_after_a_backward_refetches(tl):
+    """After a backward the ring holds the first tiles, not the ones a
+    backward starts with: the next backward fetches everything again."""
+    T, K, M, N = 160, 512, 4 * 512, 4
+    ref = run_op(tl, T, K, M, N, 1, seed=5, calls=2, persistent=False, extra_backward=True)
+    r = run_op(tl, T, K, M, N, 1, seed=5, calls=2, persistent=False, reuse=True, extra_backward=True)
+    assert _same(r.y, ref.y) and _same(r.dw, ref.dw) and _same(r.dx, ref.dx)
+    assert r.stats["bwd_reused_tiles"] == 0
+    oracle_check(r, T, K, M)
+
+
+def test_tile_reuse_needs_per_tile_mode(tl):
+    K, M, N = 512, 1024, 2
+    w, dw = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
+    op = make_op(tl, K, M, N, 1, w, dw, persistent=True)
+    assert op.stats()["persistent"] == 1
+    with pytest.raises(tl.TiledLinearError) as ei:
+        op.set_tile_reuse(True)
+    assert ei.value.status == tl.TL_ERR_INVALID
+    op.set_tile_reuse(False)
+    assert op.close() == tl.TL_OK
+    w.close()
+    dw.close()
