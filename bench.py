@@ -466,6 +466,55 @@ def profile_gemms(cfg, reps: int) -> None:
     log(f"[bench] profile-gemms: {reps} x (fwd, dW, dX over {nx} columns) at T={T} K={K} Mi={Mi}")
 
 
+def run_ffn_chain(tl, cfg, x, y_up, dx, seed: int, steps: int, dist: Dist) -> dict:
+    """The workload's layer followed by its down-projection (M -> K, N tiles of
+    K/N columns, W2 [M, K] pinned, tile-major), run as one chain: one ring and
+    one prefetcher across both operators.  A step is a chain forward plus a
+    chain backward (12 T K M FLOPs); X, Y_up and dX are the main workload's
+    device buffers."""
+    import torch
+
+    from offload_streamed_gb300 import inputs as I
+    T, K, M, N, d = cfg["T"], cfg["K"], cfg["M"], cfg["N"], cfg["d"]
+    w1, dw1 = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
+    w2, dw2 = tl.PinnedBuffer(M * K), tl.PinnedBuffer(M * K)
+    I.fill_w_host(w1.tensor, K, M, N, True, seed, device="cuda")
+    I.fill_w_host(w2.tensor, M, K, N, True, seed + 1, device="cuda")
+    ch = tl.TiledLinearChain([K, M, K], [N, N], d, [w1, w2], [dw1, dw2])
+    y_down = torch.empty(T, K, dtype=torch.bfloat16, device="cuda")
+    dy = I.make_dy(T, K, seed + 1, device="cuda")
+    ys = [y_up, y_down]
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        ch.forward(x, ys, stream=s)
+        ch.backward(x, ys, dy, dx, stream=s)
+    torch.cuda.synchronize()
+    ch.reset_stats()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        ch.forward(x, ys, stream=s)
+        ch.backward(x, ys, dy, dx, stream=s)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = dist.max(e0.elapsed_time(e1) / steps)
+    st = ch.stats()
+    ch.close()
+    for b in (w1, dw1, w2, dw2):
+        b.close()
+    flops = 12.0 * T * K * M
+    return {"value": round(dist.world * flops / (ms / 1e3) / 1e12, 2), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "steps": steps, "tiles": st["n_tiles"], "launches_per_step": st["fwd_launches"] + st["bwd_launches"],
+            "h2d_bytes_per_step": st["fwd_h2d_bytes"] + st["bwd_h2d_bytes"],
+            "d2h_bytes_per_step": st["bwd_d2h_bytes"],
+            "compute_stream_idle_pct": round(100.0 * (1.0 - (st["sum_fwd_gemm_ms"] + st["sum_bwd_dw_gemm_ms"]
+                                                              + st["sum_bwd_dx_gemm_ms"]) /
+                                                        max(st["sum_fwd_total_ms"] + st["sum_bwd_total_ms"], 1e-9)),
+                                             2),
+            "workload": f"FFN chain: up [{K}->{M}] then down [{M}->{K}], N={N} tiles each, d={d}, T={T}, "
+                        "one ring and prefetcher over both; bf16 activations between the operators"}
+
+
 # ----------------------------------------------------------------------------
 def run_ours(args, cfg, dist: Dist):
     import torch
@@ -646,6 +695,10 @@ def run_ours(args, cfg, dist: Dist):
             "h2d_bytes_per_step": rs["fwd_h2d_bytes"] + rs["bwd_h2d_bytes"],
             "what": "backward reuses the tiles still resident from forward (not the pages' method, which "
                     "refetches every tile; W unchanged between the two calls)"}
+
+    # --- the FFN chain (up- then down-projection) through one prefetcher -------
+    if not args.skip_aux and not persistent and M % K == 0:
+        out["ffn_chain"] = run_ffn_chain(tl, cfg, x, y, dx, args.seed, max(3, min(args.steps, 20)), dist)
 
     # --- CPU oracle baseline ----------------------------------------------------
     if want_cpu:

@@ -185,6 +185,63 @@ tl_status tiled_linear_reset_stats(tl_handle *h);
  * handle. */
 tl_status tiled_linear_set_tile_reuse(tl_handle *h, int32_t enable);
 
+/* --- chains of operators: one prefetcher across several linear layers -----
+ * A chain of L tiled linear operators, run in sequence by one handle:
+ * operator l computes Y_l [T, dims[l+1]] = X_l [T, dims[l]] . W_l with W_l
+ * split into n_tiles[l] column tiles, X_0 = x and X_l = Y_{l-1} (bf16).  With
+ * L = 2 and dims = {K, 4K, K} this is the FFN's up- and down-projection, the
+ * two matrices the tiling splits (tm_zero_infinity, "Memory-centric tiling:
+ * operators bigger than the device"), with no activation between them.  One
+ * ring serves every operator.  Its prefetcher follows the operator sequence
+ * (pwwt.cn/news/5430303, 关键技术三 (1) 动态预取器): the next operator's first
+ * tiles are fetched while the current one's last tiles compute, in the
+ * forward and in the backward.  Each operator obeys tiled_linear_create's
+ * shape rules for (dims[l], dims[l+1], n_tiles[l]); the host W_l and dW_l are
+ * tile-major [n_tiles[l]][dims[l]][dims[l+1]/n_tiles[l]], pinned.  A chain
+ * handle also serves tiled_linear_destroy, _last_error, _get_stats (n_tiles
+ * = all operators' tiles), _reset_stats and _set_tile_reuse.  It runs one
+ * launch per tile; tiled_linear_forward / _backward refuse it, and the
+ * chain calls refuse a single-operator handle (TL_ERR_INVALID).  L = 1 gives the same results as
+ * tiled_linear_create_tilemajor. */
+
+/* Workspace bytes for a chain (as tiled_linear_workspace_bytes, with the ring
+ * slots sized for the largest tile and d counted over all operators' tiles);
+ * 0 if the arguments are invalid. */
+size_t tiled_linear_chain_workspace_bytes(int32_t L, const int64_t *dims, const int32_t *n_tiles,
+                                          int32_t d);
+
+/* Create a chain handle.  dims has L+1 entries, n_tiles, w_host and dw_host L
+ * each; the arrays are read during the call only, the buffers they point to
+ * are used until tiled_linear_destroy.  Errors as tiled_linear_create. */
+tl_status tiled_linear_chain_create(tl_handle **out, int32_t L, const int64_t *dims,
+                                    const int32_t *n_tiles, int32_t d,
+                                    const void *const *w_host, void *const *dw_host,
+                                    void *workspace_dev, size_t workspace_bytes, int device);
+
+/* Forward through the chain: y_dev[l] (bf16 [T, dims[l+1]], ld dims[l+1])
+ * receives operator l's output, each as tiled_linear_forward computes it.
+ * Keep y_dev[0..L-2] for the backward.  Errors as tiled_linear_forward. */
+tl_status tiled_linear_chain_forward(tl_handle *h, int64_t T, const void *x_dev,
+                                     void *const *y_dev, void *stream);
+
+/* Device scratch bytes the chain backward needs: an fp32 and a bf16 buffer of
+ * T x max(dims[1..L-1]) elements (0 for L = 1). */
+size_t tiled_linear_chain_scratch_bytes(int64_t T, int32_t L, const int64_t *dims);
+
+/* Backward through the chain, operators in reverse: operator L-1 takes dy_dev
+ * (bf16 [T, dims[L]]) as its dY; operator l < L-1 takes the bf16 RNE of the
+ * fp32 dX that operator l+1 produced.  Each operator's dW_l goes to its
+ * dw_host as tiled_linear_backward writes it, and dx_dev (fp32 [T, dims[0]])
+ * receives operator 0's dX.  y_dev[0..L-2] are the forward's outputs (the
+ * inputs X_1..X_{L-1}); for L = 1 y_dev may be NULL.  scratch_dev: 256-byte
+ * aligned device memory of at least tiled_linear_chain_scratch_bytes(T, L,
+ * dims) bytes (may be NULL for L = 1), used until `stream` completes.
+ * Errors as tiled_linear_backward, TL_ERR_WORKSPACE for the scratch. */
+tl_status tiled_linear_chain_backward(tl_handle *h, int64_t T, const void *x_dev,
+                                      const void *const *y_dev, const void *dy_dev,
+                                      float *dx_dev, void *scratch_dev, size_t scratch_bytes,
+                                      void *stream);
+
 /* --- resident GEMMs: the three kernels on device-resident operands --------
  * The same kernels the engine launches per tile, for callers that already
  * hold a tile on the device.  fp32 accumulation in tensor memory; err_dev is

@@ -24,7 +24,7 @@ LIB = os.path.join(LIBDIR, "libtiled_linear.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I", INCLUDE, "-I", CSRC]
-UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu"]
+UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_cast.cu"]
 
 
 def nvcc() -> str:

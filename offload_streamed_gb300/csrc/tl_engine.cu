@@ -21,6 +21,7 @@
 // 后向传播中的重叠: gradients go back to slow memory while later operators
 // compute).
 #include "tiled_linear.h"
+#include "tl_cast.h"
 #include "tl_gemm.h"
 
 #include <cuda.h>
@@ -104,6 +105,35 @@ int32_t slots_for(int32_t N, int32_t d) {
 
 size_t tile_bytes(int64_t K, int64_t Mi) { return size_t(K) * size_t(Mi) * 2; }
 
+// One tiled linear operator of a handle: Y [T, M] = X [T, K] . W, W split into
+// N column tiles held in pinned host memory.  A handle runs one operator, or
+// a chain of them (operator l's output is operator l+1's input); `first` is
+// the index of the operator's first tile in the handle's tile order.
+struct Op {
+    Shape s;
+    const uint8_t* w_host = nullptr;
+    uint8_t* dw_host = nullptr;
+    tl_layout layout = TL_LAYOUT_TILE_MAJOR;
+    int32_t first = 0;
+};
+
+// Workspace of a handle over `ops`: the header, then d+1 ring slots and
+// min(2, tiles) staging slots, each sized for the largest tile.
+size_t ring_slot_bytes(const std::vector<Shape>& ops) {
+    size_t tb = 0;
+    for (const Shape& o : ops) tb = std::max(tb, align_up(tile_bytes(o.K, o.Mi), kAlign));
+    return tb;
+}
+int32_t total_tiles(const std::vector<Shape>& ops) {
+    int32_t n = 0;
+    for (const Shape& o : ops) n += o.N;
+    return n;
+}
+size_t workspace_for(const std::vector<Shape>& ops, int32_t d) {
+    const int32_t n = total_tiles(ops);
+    return kHeaderBytes + size_t(slots_for(n, d) + std::min(n, kMaxStage)) * ring_slot_bytes(ops);
+}
+
 constexpr int kTimingRing = 16;
 
 // Timing events of one call.  Per tile: [0] kernel-1 start, [1] kernel-1 end,
@@ -136,7 +166,10 @@ struct Phase {
 
 struct tl_handle {
     int device = 0;
-    Shape s;
+    Shape s;                 // operator 0 (the persistent mode runs single operators only)
+    std::vector<Op> ops;     // the operators, in forward order
+    bool single_api = true;  // created by tiled_linear_create[_tilemajor] (else a chain)
+    int32_t n_total = 0;     // tiles over all operators
     tl_layout layout = TL_LAYOUT_ROW_MAJOR;
     int32_t d_req = 0, d = 0, slot_cap = 0, nstage = 0;
     bool auto_pending = false;
@@ -266,31 +299,31 @@ tl_status check_usable(tl_handle* h) {
     return poll_error(h);
 }
 
-const uint8_t* w_tile_src(const tl_handle* h, int i) {
-    const Shape& s = h->s;
-    if (h->layout == TL_LAYOUT_TILE_MAJOR) return h->w_host + size_t(i) * tile_bytes(s.K, s.Mi);
-    return h->w_host + size_t(i) * size_t(s.Mi) * 2;
+const uint8_t* w_tile_src(const Op& o, int i) {
+    const Shape& s = o.s;
+    if (o.layout == TL_LAYOUT_TILE_MAJOR) return o.w_host + size_t(i) * tile_bytes(s.K, s.Mi);
+    return o.w_host + size_t(i) * size_t(s.Mi) * 2;
 }
 
-uint8_t* dw_tile_dst(const tl_handle* h, int i) {
-    const Shape& s = h->s;
-    if (h->layout == TL_LAYOUT_TILE_MAJOR) return h->dw_host + size_t(i) * tile_bytes(s.K, s.Mi);
-    return h->dw_host + size_t(i) * size_t(s.Mi) * 2;
+uint8_t* dw_tile_dst(const Op& o, int i) {
+    const Shape& s = o.s;
+    if (o.layout == TL_LAYOUT_TILE_MAJOR) return o.dw_host + size_t(i) * tile_bytes(s.K, s.Mi);
+    return o.dw_host + size_t(i) * size_t(s.Mi) * 2;
 }
 
-cudaError_t copy_w_tile(const tl_handle* h, int i, void* dst, cudaStream_t st) {
-    const Shape& s = h->s;
-    if (h->layout == TL_LAYOUT_TILE_MAJOR)
-        return cudaMemcpyAsync(dst, w_tile_src(h, i), tile_bytes(s.K, s.Mi), cudaMemcpyHostToDevice, st);
-    return cudaMemcpy2DAsync(dst, size_t(s.Mi) * 2, w_tile_src(h, i), size_t(s.M) * 2,
+cudaError_t copy_w_tile(const Op& o, int i, void* dst, cudaStream_t st) {
+    const Shape& s = o.s;
+    if (o.layout == TL_LAYOUT_TILE_MAJOR)
+        return cudaMemcpyAsync(dst, w_tile_src(o, i), tile_bytes(s.K, s.Mi), cudaMemcpyHostToDevice, st);
+    return cudaMemcpy2DAsync(dst, size_t(s.Mi) * 2, w_tile_src(o, i), size_t(s.M) * 2,
                              size_t(s.Mi) * 2, size_t(s.K), cudaMemcpyHostToDevice, st);
 }
 
-cudaError_t copy_dw_tile(const tl_handle* h, int i, const void* src, cudaStream_t st) {
-    const Shape& s = h->s;
-    if (h->layout == TL_LAYOUT_TILE_MAJOR)
-        return cudaMemcpyAsync(dw_tile_dst(h, i), src, tile_bytes(s.K, s.Mi), cudaMemcpyDeviceToHost, st);
-    return cudaMemcpy2DAsync(dw_tile_dst(h, i), size_t(s.M) * 2, src, size_t(s.Mi) * 2,
+cudaError_t copy_dw_tile(const Op& o, int i, const void* src, cudaStream_t st) {
+    const Shape& s = o.s;
+    if (o.layout == TL_LAYOUT_TILE_MAJOR)
+        return cudaMemcpyAsync(dw_tile_dst(o, i), src, tile_bytes(s.K, s.Mi), cudaMemcpyDeviceToHost, st);
+    return cudaMemcpy2DAsync(dw_tile_dst(o, i), size_t(s.M) * 2, src, size_t(s.Mi) * 2,
                              size_t(s.Mi) * 2, size_t(s.K), cudaMemcpyDeviceToHost, st);
 }
 
@@ -329,7 +362,7 @@ tl_status harvest(tl_handle* h, Phase& p, CallSlot& c, int n) {
 
 tl_status harvest_all(tl_handle* h, Phase& p) {
     for (auto& c : p.ring) {
-        tl_status st = harvest(h, p, c, h->s.N);
+        tl_status st = harvest(h, p, c, h->n_total);
         if (st != TL_OK) return st;
     }
     return TL_OK;
@@ -338,7 +371,7 @@ tl_status harvest_all(tl_handle* h, Phase& p) {
 // Slot for the next call of phase p (harvesting the call that used it last).
 CallSlot* begin_call(tl_handle* h, Phase& p, tl_status* st) {
     CallSlot& c = p.ring[p.calls % kTimingRing];
-    *st = harvest(h, p, c, h->s.N);
+    *st = harvest(h, p, c, h->n_total);
     return *st == TL_OK ? &c : nullptr;
 }
 
@@ -371,7 +404,7 @@ int take_slot(tl_handle* h) {
 tl_status finish_auto_depth(tl_handle* h) {
     if (!h->auto_pending || h->fwd.last < 0) return TL_OK;
     CallSlot& c = h->fwd.ring[h->fwd.last];
-    tl_status st = harvest(h, h->fwd, c, h->s.N);
+    tl_status st = harvest(h, h->fwd, c, h->n_total);
     if (st != TL_OK) return st;
     const double fetch = c.h2d, layer = c.gemm1;
     int32_t dnew = 1;
@@ -406,7 +439,7 @@ CUdeviceptr cuptr(const void* p) { return reinterpret_cast<CUdeviceptr>(p); }
 // dX is accumulated over pairs of tiles when the ring holds two tiles (d >= 1)
 // and the tile width splits into whole 64-deep K-blocks.  Both launch modes
 // use the same pairs, so their dX agree bit for bit.
-bool dx_pairs(const tl_handle* h) { return h->d >= 1 && h->s.N >= 2 && h->s.Mi % tl::kBlockK == 0; }
+bool dx_pairs(const tl_handle* h, const Shape& s) { return h->d >= 1 && s.N >= 2 && s.Mi % tl::kBlockK == 0; }
 
 tl::PassDesc pass_desc(const tl_handle* h, bool backward, int64_t T, uint64_t fetch_base, uint64_t stage_base) {
     tl::PassDesc d;
@@ -421,7 +454,7 @@ tl::PassDesc pass_desc(const tl_handle* h, bool backward, int64_t T, uint64_t fe
     for (int g = 0; g < d.nstage && g < tl::kMaxPassStages; ++g) d.stages[g] = h->stage[g];
     d.fetch_base = uint32_t(fetch_base);
     d.stage_base = uint32_t(stage_base);
-    d.dx_group = dx_pairs(h) ? 2 : 1;
+    d.dx_group = dx_pairs(h, h->s) ? 2 : 1;
     d.flags = h->flags;
     d.done = h->done;
     d.dwdone = h->dwdone;
@@ -443,7 +476,7 @@ tl_status enqueue_fetches(tl_handle* h, CallSlot& t, uint64_t base, bool backwar
         if (f >= nslots)
             TL_CU(h, mo.wait(cu(h->h2d), cuptr(h->flags + tl::kFlagFreed + sl), uint32_t(f - nslots + 1), kWaitGeq));
         TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
-        TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
+        TL_TRY(h, copy_w_tile(h->ops[0], i, h->slot[sl], h->h2d));
         TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
         TL_CU(h, mo.write(cu(h->h2d), cuptr(h->flags + tl::kFlagReady + sl), uint32_t(f + 1), kWriteDefault));
     }
@@ -463,22 +496,37 @@ tl_status launch(tl_handle* h, const tl::GemmDesc& g, cudaStream_t st) {
     return TL_OK;
 }
 
-tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t d,
-                      const void* w_host, void* dw_host, void* ws, size_t ws_bytes, int device,
-                      tl_layout layout) {
+// Create a handle over `ops` (one operator, or a chain) sharing one ring.
+tl_status create_ops(tl_handle** out, std::vector<Op> ops, int32_t d, void* ws, size_t ws_bytes, int device,
+                     bool single_api) {
     if (!out) {
         g_create_error = "out is NULL";
         return TL_ERR_INVALID;
     }
     *out = nullptr;
-    std::string bad = check_shape(K, M, N, d);
-    if (bad.empty() && (!w_host || !dw_host || !ws)) bad = "null pointer argument";
+    std::string bad = ops.empty() ? "no operators" : "";
+    std::vector<Shape> shapes;
+    int32_t first = 0;
+    for (size_t l = 0; l < ops.size() && bad.empty(); ++l) {
+        Op& o = ops[l];
+        bad = check_shape(o.s.K, o.s.M, o.s.N, d);
+        if (bad.empty() && (!o.w_host || !o.dw_host)) bad = "null pointer argument";
+        if (bad.empty() && l > 0 && o.s.K != ops[l - 1].s.M) bad = "operator inputs must match the outputs before them";
+        if (!bad.empty() && ops.size() > 1) bad = "operator " + std::to_string(l) + ": " + bad;
+        o.s.Mi = o.s.M / std::max<int32_t>(o.s.N, 1);
+        o.first = first;
+        first += o.s.N;
+        shapes.push_back(o.s);
+    }
+    if (bad.empty() && first > (1 << 20)) bad = "too many tiles";
+    if (bad.empty() && !ws) bad = "null pointer argument";
     if (bad.empty() && device < 0) bad = "device must be >= 0";
     if (!bad.empty()) {
         g_create_error = bad;
         return TL_ERR_INVALID;
     }
-    const size_t need = tiled_linear_workspace_bytes(K, M, N, d);
+    const int32_t N = first;  // tiles over all operators
+    const size_t need = workspace_for(shapes, d);
     if (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % kAlign)) {
         g_create_error = "workspace too small or not 256-byte aligned (need " + std::to_string(need) +
                          " bytes)";
@@ -496,14 +544,14 @@ tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t 
         return st;
     };
     h->device = device;
-    h->s.K = K;
-    h->s.M = M;
-    h->s.N = N;
-    h->s.Mi = M / N;
-    h->layout = layout;
+    h->ops = ops;
+    h->single_api = single_api;
+    h->n_total = N;
+    h->s = ops[0].s;
+    h->layout = ops[0].layout;
     h->d_req = d;
-    h->w_host = static_cast<const uint8_t*>(w_host);
-    h->dw_host = static_cast<uint8_t*>(dw_host);
+    h->w_host = ops[0].w_host;
+    h->dw_host = ops[0].dw_host;
     h->ws = static_cast<uint8_t*>(ws);
     h->ws_bytes = ws_bytes;
 
@@ -512,17 +560,18 @@ tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t 
         h->msg = std::string("cudaSetDevice: ") + cudaGetErrorString(guard.err);
         return bail(TL_ERR_CUDA);
     }
-    if (!is_pinned_host(w_host) || !is_pinned_host(dw_host)) {
-        h->msg = "w_host and dw_host must be pinned host memory";
-        return bail(TL_ERR_NOT_PINNED);
-    }
+    for (const Op& o : ops)
+        if (!is_pinned_host(o.w_host) || !is_pinned_host(o.dw_host)) {
+            h->msg = "w_host and dw_host must be pinned host memory";
+            return bail(TL_ERR_NOT_PINNED);
+        }
     if (!is_device_mem(ws, device)) {
         h->msg = "workspace is not device memory of the handle's device";
         return bail(TL_ERR_WORKSPACE);
     }
 
     // Carve the workspace: header (error word), weight slots, staging slots.
-    const size_t tb = align_up(tile_bytes(K, M / N), kAlign);
+    const size_t tb = ring_slot_bytes(shapes);
     const int32_t min_slots = slots_for(N, d);
     const int32_t fit = int32_t(std::min<size_t>(size_t(N), (ws_bytes - kHeaderBytes) / tb - size_t(std::min(N, kMaxStage))));
     h->nstage = std::min(N, kMaxStage);
@@ -588,7 +637,7 @@ tl_status create_impl(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t 
         probe.x = h->ws;
         probe.y = h->ws;
         const MemOps& mo = memops();
-        if (wanted && mo.write && mo.wait && tl::pass_check(probe, h->num_sms).empty()) {
+        if (wanted && single_api && mo.write && mo.wait && tl::pass_check(probe, h->num_sms).empty()) {
             // the stream memory operations must work on this device
             if (mo.write(cu(h->h2d), cuptr(h->flags + tl::kNumFlags), 0u, kWriteDefault) == CUDA_SUCCESS &&
                 cudaStreamSynchronize(h->h2d) == cudaSuccess && tl::pass_preload() == cudaSuccess)
@@ -648,7 +697,7 @@ tl_status backward_persistent(tl_handle* h, int64_t T, const void* x, const void
         TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_call_done, 0));
         TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_d2h_tail, 0));
         TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tb, cs));
-        for (int i = 0; i < s.N; ++i) TL_TRY(h, copy_dw_tile(h, i, h->stage[0], cs));
+        for (int i = 0; i < s.N; ++i) TL_TRY(h, copy_dw_tile(h->ops[0], i, h->stage[0], cs));
         TL_TRY(h, cudaEventRecord(h->ev_call_done, cs));
         return TL_OK;
     }
@@ -677,7 +726,7 @@ tl_status backward_persistent(tl_handle* h, int64_t T, const void* x, const void
         const int g = int(sj % uint64_t(h->nstage));
         TL_CU(h, mo.wait(cu(h->d2h), cuptr(h->flags + tl::kFlagDwReady + g), uint32_t(sj + 1), kWaitGeq));
         TL_TRY(h, cudaEventRecord(t.ev[6][j], h->d2h));
-        TL_TRY(h, copy_dw_tile(h, i, h->stage[g], h->d2h));
+        TL_TRY(h, copy_dw_tile(h->ops[0], i, h->stage[g], h->d2h));
         TL_TRY(h, cudaEventRecord(t.ev[7][j], h->d2h));
         TL_CU(h, mo.write(cu(h->d2h), cuptr(h->flags + tl::kFlagDrained + g), uint32_t(sj + 1), kWriteDefault));
     }
@@ -695,246 +744,403 @@ tl_status backward_persistent(tl_handle* h, int64_t T, const void* x, const void
     return TL_OK;
 }
 
+// ---- one launch per tile, over the handle's operators in sequence ----------
+// Forward: operator l computes ys[l][:, tile i] = X_l . W_{l,i}, X_0 = x and
+// X_l = ys[l-1]; the ring streams the operators' tiles in that order, so the
+// next operator's first tiles are fetched while this one's last tiles run.
+tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys, cudaStream_t cs) {
+    tl_status st;
+    CallSlot* tp = begin_call(h, h->fwd, &st);
+    if (!tp) return st;
+    CallSlot& t = *tp;
+    int64_t h2d_bytes = 0;
+    TL_TRY(h, cudaEventRecord(t.start, cs));
+    for (size_t l = 0; l < h->ops.size(); ++l) {
+        const Op& o = h->ops[l];
+        const Shape& s = o.s;
+        const void* xl = l == 0 ? x : ys[l - 1];
+        for (int i = 0; i < s.N; ++i) {
+            const int g = o.first + i;  // tile index in the handle's order
+            const int sl = take_slot(h);
+            if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
+            h->slot_tile[size_t(sl)] = -1;
+            TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
+            TL_TRY(h, cudaEventRecord(t.ev[4][g], h->h2d));
+            TL_TRY(h, copy_w_tile(o, i, h->slot[sl], h->h2d));
+            h->slot_tile[size_t(sl)] = g;
+            h2d_bytes += int64_t(tile_bytes(s.K, s.Mi));
+            TL_TRY(h, cudaEventRecord(t.ev[5][g], h->h2d));
+            TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
+
+            TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
+            TL_TRY(h, cudaEventRecord(t.ev[0][g], cs));
+            tl::GemmDesc gd;
+            gd.m_dim = T;
+            gd.n_dim = s.Mi;
+            gd.k_dim = s.K;
+            gd.a = xl;
+            gd.lda = s.K;
+            gd.a_mn_major = false;
+            gd.b = h->slot[sl];
+            gd.ldb = s.Mi;
+            gd.b_mn_major = true;
+            gd.d = static_cast<uint8_t*>(ys[l]) + size_t(i) * size_t(s.Mi) * 2;
+            gd.ldd = s.M;
+            gd.out = tl::OutKind::BF16;
+            gd.err = h->err_dev;
+            if ((st = launch(h, gd, cs)) != TL_OK) return st;
+            TL_TRY(h, cudaEventRecord(t.ev[1][g], cs));
+            TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
+            h->slot_q.push_back(sl);
+        }
+    }
+    TL_TRY(h, cudaEventRecord(t.end, cs));
+    TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    t.nk = h->n_total;
+    t.depth = h->d;
+    t.launches = h->n_total;
+    t.h2d_bytes = h2d_bytes;
+    t.d2h_bytes = 0;
+    end_call(h->fwd, t);
+    return TL_OK;
+}
+
+// Backward, operators in reverse and each one's tiles in descending order:
+//   dW_{l,i} = X_l^T . dY_l[:, tile i] -> staging slot -> host (d2h stream)
+//   dX_l (+)= dY_l[:, tile i] . W_{l,i}^T in fp32 (tile pairs, see dx_pairs)
+// dY_{L-1} = dy; for l < L-1, dY_l = bf16(dX_{l+1}) (cast on the caller's
+// stream into scr_dy), dX_l for l >= 1 accumulates in scr_dx, dX_0 in dx.
+tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* const* ys, const void* dy,
+                         float* dx, float* scr_dx, void* scr_dy, cudaStream_t cs) {
+    tl_status st;
+    const int L = int(h->ops.size());
+    if (T == 0) {  // dW = X^T dY over an empty sum: zero
+        for (const Op& o : h->ops) {
+            TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[0], 0));
+            TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tile_bytes(o.s.K, o.s.Mi), cs));
+            for (int i = 0; i < o.s.N; ++i) TL_TRY(h, copy_dw_tile(o, i, h->stage[0], cs));
+            TL_TRY(h, cudaEventRecord(h->ev_drained[0], cs));
+        }
+        return TL_OK;
+    }
+    CallSlot* tp = begin_call(h, h->bwd, &st);
+    if (!tp) return st;
+    CallSlot& t = *tp;
+    const int NT = h->n_total;
+    // With reuse on, the longest prefix of the descending tile order that is
+    // still resident in the ring (the last d+1 tiles a forward fetched) is
+    // taken as it is; those slots leave the free queue until their dX launch.
+    std::vector<int> resident(size_t(NT), -1);
+    int reused = 0;
+    if (h->reuse) {
+        for (int sl = 0; sl <= h->d; ++sl)
+            if (h->slot_tile[size_t(sl)] >= 0) resident[size_t(h->slot_tile[size_t(sl)])] = sl;
+        while (reused < NT && resident[size_t(NT - 1 - reused)] >= 0) ++reused;
+        std::deque<int> q;
+        for (int sl : h->slot_q) {
+            bool taken = false;
+            for (int j = 0; j < reused; ++j) taken = taken || resident[size_t(NT - 1 - j)] == sl;
+            if (!taken) q.push_back(sl);
+        }
+        h->slot_q.swap(q);
+    }
+    int64_t h2d_bytes = 0, d2h_bytes = 0;
+    int launches = 0;
+    int jg = 0;  // position in the backward's tile order
+    TL_TRY(h, cudaEventRecord(t.start, cs));
+    for (int l = L - 1; l >= 0; --l) {
+        const Op& o = h->ops[size_t(l)];
+        const Shape& s = o.s;
+        const void* xl = l == 0 ? x : ys[l - 1];
+        const void* dyl = l == L - 1 ? dy : scr_dy;
+        float* dxl = l == 0 ? dx : scr_dx;
+        const size_t tb = tile_bytes(s.K, s.Mi);
+        // dX is accumulated over pairs of tiles (i+1, i) -- one launch
+        // reducing over both, in ascending column order -- whenever the ring
+        // holds two tiles; a lone last tile (N odd) and d = 0 go one at a time.
+        const bool pairs = dx_pairs(h, s);
+        int pend_sl = -1;  // ring slot of the pair's first (higher) tile
+        int dx_launches = 0;
+        for (int j = 0; j < s.N; ++j, ++jg) {
+            const int i = s.N - 1 - j;
+            const int g = o.first + i;
+            const int gs = int(h->stage_seq++ % uint64_t(h->nstage));
+            int sl;
+            if (jg < reused) {  // W_i is still in the ring
+                sl = resident[size_t(g)];
+                TL_TRY(h, cudaEventRecord(t.ev[4][jg], h->h2d));
+                TL_TRY(h, cudaEventRecord(t.ev[5][jg], h->h2d));
+            } else {  // refetch W_i
+                sl = take_slot(h);
+                if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
+                h->slot_tile[size_t(sl)] = -1;
+                TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
+                TL_TRY(h, cudaEventRecord(t.ev[4][jg], h->h2d));
+                TL_TRY(h, copy_w_tile(o, i, h->slot[sl], h->h2d));
+                TL_TRY(h, cudaEventRecord(t.ev[5][jg], h->h2d));
+                TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
+                h->slot_tile[size_t(sl)] = g;
+                h2d_bytes += int64_t(tb);
+            }
+
+            // dW_i = X^T dY_i into staging slot gs (does not need W_i)
+            TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gs], 0));
+            TL_TRY(h, cudaEventRecord(t.ev[0][jg], cs));
+            tl::GemmDesc gw;
+            gw.m_dim = s.K;
+            gw.n_dim = s.Mi;
+            gw.k_dim = T;
+            gw.a = xl;
+            gw.lda = s.K;
+            gw.a_mn_major = true;
+            gw.b = static_cast<const uint8_t*>(dyl) + size_t(i) * size_t(s.Mi) * 2;
+            gw.ldb = s.M;
+            gw.b_mn_major = true;
+            gw.d = h->stage[gs];
+            gw.ldd = s.Mi;
+            gw.out = tl::OutKind::BF16;
+            gw.err = h->err_dev;
+            if ((st = launch(h, gw, cs)) != TL_OK) return st;
+            ++launches;
+            TL_TRY(h, cudaEventRecord(t.ev[1][jg], cs));
+            TL_TRY(h, cudaEventRecord(h->ev_dwdone[gs], cs));
+
+            // write dW_i back on the d2h stream
+            TL_TRY(h, cudaStreamWaitEvent(h->d2h, h->ev_dwdone[gs], 0));
+            TL_TRY(h, cudaEventRecord(t.ev[6][jg], h->d2h));
+            TL_TRY(h, copy_dw_tile(o, i, h->stage[gs], h->d2h));
+            TL_TRY(h, cudaEventRecord(t.ev[7][jg], h->d2h));
+            TL_TRY(h, cudaEventRecord(h->ev_drained[gs], h->d2h));
+            d2h_bytes += int64_t(tb);
+
+            if (pairs && pend_sl < 0 && j + 1 < s.N) {
+                // first tile of a pair: its dX is reduced with the next tile's
+                pend_sl = sl;
+                TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
+                TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
+                continue;
+            }
+            // dX (+)= dY_i W_i^T (+ dY_{i+1} W_{i+1}^T), fp32; the first launch stores
+            TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
+            if (pend_sl >= 0) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[pend_sl], 0));
+            TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
+            tl::GemmDesc gx;
+            gx.m_dim = T;
+            gx.n_dim = s.K;
+            gx.k_dim = pend_sl >= 0 ? 2 * s.Mi : s.Mi;
+            gx.a = static_cast<const uint8_t*>(dyl) + size_t(i) * size_t(s.Mi) * 2;
+            gx.lda = s.M;
+            gx.a_mn_major = false;
+            gx.b = h->slot[sl];
+            gx.ldb = s.Mi;
+            gx.b_mn_major = false;
+            if (pend_sl >= 0) {  // reduction rows Mi .. 2Mi-1 are tile i+1's
+                gx.b2 = h->slot[pend_sl];
+                gx.k_split = s.Mi;
+            }
+            gx.d = dxl;
+            gx.ldd = s.K;
+            gx.out = tl::OutKind::F32;
+            gx.accumulate = dx_launches > 0;
+            gx.err = h->err_dev;
+            if ((st = launch(h, gx, cs)) != TL_OK) return st;
+            ++dx_launches;
+            ++launches;
+            TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
+            TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
+            if (pend_sl >= 0) {
+                TL_TRY(h, cudaEventRecord(h->ev_free[pend_sl], cs));
+                h->slot_q.push_back(pend_sl);
+            }
+            h->slot_q.push_back(sl);
+            pend_sl = -1;
+        }
+        if (l > 0) {  // dY of the operator before: bf16 RNE of this dX
+            std::string why;
+            if (tl::cast_f32_bf16(scr_dx, scr_dy, T * s.K, h->num_sms, cs, &why) != cudaSuccess)
+                return fail(h, TL_ERR_CUDA, "dX -> dY cast: " + why);
+            ++launches;
+        }
+    }
+    // dW on the host is complete when `stream` is.
+    for (int gi = 0; gi < h->nstage; ++gi) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gi], 0));
+    TL_TRY(h, cudaEventRecord(t.end, cs));
+    TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    t.nk = NT;
+    t.depth = h->d;
+    t.launches = launches;
+    t.reused = reused;
+    t.h2d_bytes = h2d_bytes;
+    t.d2h_bytes = d2h_bytes;
+    end_call(h->bwd, t);
+    return TL_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t tiled_linear_workspace_bytes(int64_t K, int64_t M, int32_t N, int32_t d) {
     if (!check_shape(K, M, N, d).empty()) return 0;
-    const size_t tb = align_up(tile_bytes(K, M / N), kAlign);
-    return kHeaderBytes + size_t(slots_for(N, d) + std::min(N, kMaxStage)) * tb;
+    return workspace_for({Shape{K, M, M / N, N}}, d);
+}
+
+static Op one_op(int64_t K, int64_t M, int32_t N, const void* w_host, void* dw_host, tl_layout layout) {
+    Op o;
+    o.s = Shape{K, M, N > 0 ? M / N : 0, N};
+    o.w_host = static_cast<const uint8_t*>(w_host);
+    o.dw_host = static_cast<uint8_t*>(dw_host);
+    o.layout = layout;
+    return o;
 }
 
 tl_status tiled_linear_create(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t d,
                               const void* w_host, void* dw_host, void* workspace_dev,
                               size_t workspace_bytes, int device) {
-    return create_impl(out, K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes, device,
-                       TL_LAYOUT_ROW_MAJOR);
+    return create_ops(out, {one_op(K, M, N, w_host, dw_host, TL_LAYOUT_ROW_MAJOR)}, d, workspace_dev,
+                      workspace_bytes, device, true);
 }
 
 tl_status tiled_linear_create_tilemajor(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t d,
                                         const void* w_host, void* dw_host, void* workspace_dev,
                                         size_t workspace_bytes, int device) {
-    return create_impl(out, K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes, device,
-                       TL_LAYOUT_TILE_MAJOR);
+    return create_ops(out, {one_op(K, M, N, w_host, dw_host, TL_LAYOUT_TILE_MAJOR)}, d, workspace_dev,
+                      workspace_bytes, device, true);
 }
 
-tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void* y_dev, void* stream) {
+static std::string chain_args(int32_t L, const int64_t* dims, const int32_t* n_tiles) {
+    if (L < 1 || L > 64) return "L must be in 1..64";
+    if (!dims || !n_tiles) return "null dims or n_tiles";
+    return {};
+}
+
+size_t tiled_linear_chain_workspace_bytes(int32_t L, const int64_t* dims, const int32_t* n_tiles, int32_t d) {
+    if (!chain_args(L, dims, n_tiles).empty()) return 0;
+    std::vector<Shape> shapes;
+    for (int l = 0; l < L; ++l) {
+        if (!check_shape(dims[l], dims[l + 1], n_tiles[l], d).empty()) return 0;
+        shapes.push_back(Shape{dims[l], dims[l + 1], dims[l + 1] / n_tiles[l], n_tiles[l]});
+    }
+    return workspace_for(shapes, d);
+}
+
+tl_status tiled_linear_chain_create(tl_handle** out, int32_t L, const int64_t* dims, const int32_t* n_tiles,
+                                    int32_t d, const void* const* w_host, void* const* dw_host,
+                                    void* workspace_dev, size_t workspace_bytes, int device) {
+    std::string bad = chain_args(L, dims, n_tiles);
+    if (bad.empty() && (!w_host || !dw_host)) bad = "null w_host or dw_host array";
+    if (!bad.empty()) {
+        g_create_error = bad;
+        if (out) *out = nullptr;
+        return TL_ERR_INVALID;
+    }
+    std::vector<Op> ops;
+    for (int l = 0; l < L; ++l)
+        ops.push_back(one_op(dims[l], dims[l + 1], n_tiles[l], w_host[l], dw_host[l], TL_LAYOUT_TILE_MAJOR));
+    return create_ops(out, ops, d, workspace_dev, workspace_bytes, device, false);
+}
+
+// Shared argument checks of the call entry points.  Returns TL_OK or the
+// status to return (with the handle's message set).
+static tl_status call_prologue(tl_handle* h, int64_t T) {
     tl_status st = check_usable(h);
     if (st != TL_OK) return st;
     if (T < 0 || T > (int64_t(1) << 30)) return fail(h, TL_ERR_INVALID, "T out of range");
+    return TL_OK;
+}
+
+static bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+tl_status tiled_linear_forward(tl_handle* h, int64_t T, const void* x_dev, void* y_dev, void* stream) {
+    tl_status st = call_prologue(h, T);
+    if (st != TL_OK) return st;
+    if (!h->single_api) return fail(h, TL_ERR_INVALID, "a chain handle runs tiled_linear_chain_forward");
     if (T == 0) return TL_OK;
     if (!x_dev || !y_dev) return fail(h, TL_ERR_INVALID, "null x or y");
-    if ((reinterpret_cast<uintptr_t>(x_dev) | reinterpret_cast<uintptr_t>(y_dev)) & 15u)
-        return fail(h, TL_ERR_INVALID, "x and y must be 16-byte aligned");
+    if (misaligned(x_dev) || misaligned(y_dev)) return fail(h, TL_ERR_INVALID, "x and y must be 16-byte aligned");
     DeviceGuard guard(h->device);
     if (guard.err != cudaSuccess) return fail(h, TL_ERR_CUDA, "cudaSetDevice failed");
     if ((st = finish_auto_depth(h)) != TL_OK) return st;
-
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (h->persistent) return forward_persistent(h, T, x_dev, y_dev, cs);
-    const Shape& s = h->s;
-    CallSlot* tp = begin_call(h, h->fwd, &st);
-    if (!tp) return st;
-    CallSlot& t = *tp;
-    TL_TRY(h, cudaEventRecord(t.start, cs));
-    for (int i = 0; i < s.N; ++i) {
-        const int sl = take_slot(h);
-        if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
-        h->slot_tile[size_t(sl)] = -1;
-        TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
-        TL_TRY(h, cudaEventRecord(t.ev[4][i], h->h2d));
-        TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
-        h->slot_tile[size_t(sl)] = i;
-        TL_TRY(h, cudaEventRecord(t.ev[5][i], h->h2d));
-        TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
-
-        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
-        TL_TRY(h, cudaEventRecord(t.ev[0][i], cs));
-        tl::GemmDesc g;
-        g.m_dim = T;
-        g.n_dim = s.Mi;
-        g.k_dim = s.K;
-        g.a = x_dev;
-        g.lda = s.K;
-        g.a_mn_major = false;
-        g.b = h->slot[sl];
-        g.ldb = s.Mi;
-        g.b_mn_major = true;
-        g.d = static_cast<uint8_t*>(y_dev) + size_t(i) * size_t(s.Mi) * 2;
-        g.ldd = s.M;
-        g.out = tl::OutKind::BF16;
-        g.err = h->err_dev;
-        if ((st = launch(h, g, cs)) != TL_OK) return st;
-        TL_TRY(h, cudaEventRecord(t.ev[1][i], cs));
-        TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
-        h->slot_q.push_back(sl);
-    }
-    TL_TRY(h, cudaEventRecord(t.end, cs));
-    TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
-    t.nk = s.N;
-    t.depth = h->d;
-    t.launches = s.N;
-    t.h2d_bytes = int64_t(s.N) * int64_t(tile_bytes(s.K, s.Mi));
-    t.d2h_bytes = 0;
-    end_call(h->fwd, t);
-    return TL_OK;
+    void* ys[1] = {y_dev};
+    return forward_tiles(h, T, x_dev, ys, cs);
 }
 
 tl_status tiled_linear_backward(tl_handle* h, int64_t T, const void* x_dev, const void* dy_dev,
                                 float* dx_dev, void* stream) {
-    tl_status st = check_usable(h);
+    tl_status st = call_prologue(h, T);
     if (st != TL_OK) return st;
-    if (T < 0 || T > (int64_t(1) << 30)) return fail(h, TL_ERR_INVALID, "T out of range");
+    if (!h->single_api) return fail(h, TL_ERR_INVALID, "a chain handle runs tiled_linear_chain_backward");
     if (T > 0 && (!x_dev || !dy_dev || !dx_dev)) return fail(h, TL_ERR_INVALID, "null x, dy or dx");
-    if ((reinterpret_cast<uintptr_t>(x_dev) | reinterpret_cast<uintptr_t>(dy_dev) |
-         reinterpret_cast<uintptr_t>(dx_dev)) & 15u)
+    if (misaligned(x_dev) || misaligned(dy_dev) || misaligned(dx_dev))
         return fail(h, TL_ERR_INVALID, "x, dy and dx must be 16-byte aligned");
     DeviceGuard guard(h->device);
     if (guard.err != cudaSuccess) return fail(h, TL_ERR_CUDA, "cudaSetDevice failed");
     if ((st = finish_auto_depth(h)) != TL_OK) return st;
-
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (h->persistent) return backward_persistent(h, T, x_dev, dy_dev, dx_dev, cs);
-    const Shape& s = h->s;
-    const size_t tb = tile_bytes(s.K, s.Mi);
+    return backward_tiles(h, T, x_dev, nullptr, dy_dev, dx_dev, nullptr, nullptr, cs);
+}
 
-    if (T == 0) {  // dW = X^T dY over an empty sum: zero
-        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[0], 0));
-        TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tb, cs));
-        for (int i = 0; i < s.N; ++i) TL_TRY(h, copy_dw_tile(h, i, h->stage[0], cs));
-        TL_TRY(h, cudaEventRecord(h->ev_drained[0], cs));
-        return TL_OK;
+size_t tiled_linear_chain_scratch_bytes(int64_t T, int32_t L, const int64_t* dims) {
+    if (T < 0 || L < 1 || !dims) return 0;
+    int64_t inner = 0;
+    for (int l = 1; l < L; ++l) inner = std::max(inner, dims[l]);
+    if (inner == 0) return 0;
+    return align_up(size_t(T) * size_t(inner) * 4, kAlign) + align_up(size_t(T) * size_t(inner) * 2, kAlign);
+}
+
+tl_status tiled_linear_chain_forward(tl_handle* h, int64_t T, const void* x_dev, void* const* y_dev,
+                                     void* stream) {
+    tl_status st = call_prologue(h, T);
+    if (st != TL_OK) return st;
+    if (h->single_api) return fail(h, TL_ERR_INVALID, "a single-operator handle runs tiled_linear_forward");
+    if (T == 0) return TL_OK;
+    if (!x_dev || !y_dev || misaligned(x_dev)) return fail(h, TL_ERR_INVALID, "null or misaligned x / y array");
+    for (size_t l = 0; l < h->ops.size(); ++l)
+        if (!y_dev[l] || misaligned(y_dev[l]))
+            return fail(h, TL_ERR_INVALID, "y[" + std::to_string(l) + "] is null or not 16-byte aligned");
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return fail(h, TL_ERR_CUDA, "cudaSetDevice failed");
+    if ((st = finish_auto_depth(h)) != TL_OK) return st;
+    return forward_tiles(h, T, x_dev, y_dev, static_cast<cudaStream_t>(stream));
+}
+
+tl_status tiled_linear_chain_backward(tl_handle* h, int64_t T, const void* x_dev, const void* const* y_dev,
+                                      const void* dy_dev, float* dx_dev, void* scratch_dev,
+                                      size_t scratch_bytes, void* stream) {
+    tl_status st = call_prologue(h, T);
+    if (st != TL_OK) return st;
+    if (h->single_api) return fail(h, TL_ERR_INVALID, "a single-operator handle runs tiled_linear_backward");
+    const int L = int(h->ops.size());
+    float* scr_dx = nullptr;
+    void* scr_dy = nullptr;
+    if (T > 0) {
+        if (!x_dev || !dy_dev || !dx_dev || misaligned(x_dev) || misaligned(dy_dev) || misaligned(dx_dev))
+            return fail(h, TL_ERR_INVALID, "x, dy and dx must be non-null and 16-byte aligned");
+        if (L > 1) {
+            if (!y_dev) return fail(h, TL_ERR_INVALID, "null y array");
+            for (int l = 0; l + 1 < L; ++l)
+                if (!y_dev[l] || misaligned(y_dev[l]))
+                    return fail(h, TL_ERR_INVALID, "y[" + std::to_string(l) + "] is null or not 16-byte aligned");
+            std::vector<int64_t> dims;
+            dims.push_back(h->ops[0].s.K);
+            for (const Op& o : h->ops) dims.push_back(o.s.M);
+            const size_t need = tiled_linear_chain_scratch_bytes(T, L, dims.data());
+            if (!scratch_dev || scratch_bytes < need || (reinterpret_cast<uintptr_t>(scratch_dev) % kAlign))
+                return fail(h, TL_ERR_WORKSPACE, "scratch too small or not 256-byte aligned (need " +
+                                                     std::to_string(need) + " bytes)");
+            int64_t inner = 0;
+            for (int l = 1; l < L; ++l) inner = std::max(inner, dims[size_t(l)]);
+            scr_dx = static_cast<float*>(scratch_dev);
+            scr_dy = static_cast<uint8_t*>(scratch_dev) + align_up(size_t(T) * size_t(inner) * 4, kAlign);
+        }
     }
-
-    CallSlot* tp = begin_call(h, h->bwd, &st);
-    if (!tp) return st;
-    CallSlot& t = *tp;
-    // With reuse on, the longest prefix of the descending tile order that is
-    // still resident in the ring (the last d+1 tiles a forward fetched) is
-    // taken as it is; those slots leave the free queue until their dX launch.
-    std::vector<int> resident(size_t(s.N), -1);
-    int reused = 0;
-    if (h->reuse) {
-        for (int sl = 0; sl <= h->d; ++sl)
-            if (h->slot_tile[size_t(sl)] >= 0) resident[size_t(h->slot_tile[size_t(sl)])] = sl;
-        while (reused < s.N && resident[size_t(s.N - 1 - reused)] >= 0) ++reused;
-        std::deque<int> q;
-        for (int sl : h->slot_q) {
-            bool taken = false;
-            for (int j = 0; j < reused; ++j) taken = taken || resident[size_t(s.N - 1 - j)] == sl;
-            if (!taken) q.push_back(sl);
-        }
-        h->slot_q.swap(q);
-    }
-    // dX is accumulated over pairs of tiles (i+1, i) -- one launch reducing
-    // over both, in ascending column order -- whenever the ring holds two
-    // tiles; a lone last tile (N odd) and d = 0 go one tile at a time.
-    const bool pairs = dx_pairs(h);
-    int pend_sl = -1;  // ring slot of the pair's first (higher) tile
-    int dx_launches = 0;
-    TL_TRY(h, cudaEventRecord(t.start, cs));
-    for (int j = 0; j < s.N; ++j) {
-        const int i = s.N - 1 - j;
-        const int gs = int(h->stage_seq++ % uint64_t(h->nstage));
-        int sl;
-        if (j < reused) {  // W_i is still in the ring
-            sl = resident[size_t(i)];
-            TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
-            TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
-        } else {  // refetch W_i
-            sl = take_slot(h);
-            if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
-            h->slot_tile[size_t(sl)] = -1;
-            TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
-            TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
-            TL_TRY(h, copy_w_tile(h, i, h->slot[sl], h->h2d));
-            TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
-            TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
-            h->slot_tile[size_t(sl)] = i;
-        }
-
-        // dW_i = X^T dY_i into staging slot gs (does not need W_i)
-        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gs], 0));
-        TL_TRY(h, cudaEventRecord(t.ev[0][j], cs));
-        tl::GemmDesc gw;
-        gw.m_dim = s.K;
-        gw.n_dim = s.Mi;
-        gw.k_dim = T;
-        gw.a = x_dev;
-        gw.lda = s.K;
-        gw.a_mn_major = true;
-        gw.b = static_cast<const uint8_t*>(dy_dev) + size_t(i) * size_t(s.Mi) * 2;
-        gw.ldb = s.M;
-        gw.b_mn_major = true;
-        gw.d = h->stage[gs];
-        gw.ldd = s.Mi;
-        gw.out = tl::OutKind::BF16;
-        gw.err = h->err_dev;
-        if ((st = launch(h, gw, cs)) != TL_OK) return st;
-        TL_TRY(h, cudaEventRecord(t.ev[1][j], cs));
-        TL_TRY(h, cudaEventRecord(h->ev_dwdone[gs], cs));
-
-        // write dW_i back on the d2h stream
-        TL_TRY(h, cudaStreamWaitEvent(h->d2h, h->ev_dwdone[gs], 0));
-        TL_TRY(h, cudaEventRecord(t.ev[6][j], h->d2h));
-        TL_TRY(h, copy_dw_tile(h, i, h->stage[gs], h->d2h));
-        TL_TRY(h, cudaEventRecord(t.ev[7][j], h->d2h));
-        TL_TRY(h, cudaEventRecord(h->ev_drained[gs], h->d2h));
-
-        if (pairs && pend_sl < 0 && j + 1 < s.N) {
-            // first tile of a pair: its dX is reduced with the next tile's
-            pend_sl = sl;
-            TL_TRY(h, cudaEventRecord(t.ev[2][j], cs));
-            TL_TRY(h, cudaEventRecord(t.ev[3][j], cs));
-            continue;
-        }
-        // dX (+)= dY_i W_i^T (+ dY_{i+1} W_{i+1}^T), fp32; the first launch stores
-        TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
-        if (pend_sl >= 0) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[pend_sl], 0));
-        TL_TRY(h, cudaEventRecord(t.ev[2][j], cs));
-        tl::GemmDesc gx;
-        gx.m_dim = T;
-        gx.n_dim = s.K;
-        gx.k_dim = pend_sl >= 0 ? 2 * s.Mi : s.Mi;
-        gx.a = static_cast<const uint8_t*>(dy_dev) + size_t(i) * size_t(s.Mi) * 2;
-        gx.lda = s.M;
-        gx.a_mn_major = false;
-        gx.b = h->slot[sl];
-        gx.ldb = s.Mi;
-        gx.b_mn_major = false;
-        if (pend_sl >= 0) {  // reduction rows Mi .. 2Mi-1 are tile i+1's
-            gx.b2 = h->slot[pend_sl];
-            gx.k_split = s.Mi;
-        }
-        gx.d = dx_dev;
-        gx.ldd = s.K;
-        gx.out = tl::OutKind::F32;
-        gx.accumulate = dx_launches > 0;
-        gx.err = h->err_dev;
-        if ((st = launch(h, gx, cs)) != TL_OK) return st;
-        ++dx_launches;
-        TL_TRY(h, cudaEventRecord(t.ev[3][j], cs));
-        TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
-        if (pend_sl >= 0) {
-            TL_TRY(h, cudaEventRecord(h->ev_free[pend_sl], cs));
-            h->slot_q.push_back(pend_sl);
-        }
-        h->slot_q.push_back(sl);
-        pend_sl = -1;
-    }
-    // dW on the host is complete when `stream` is.
-    for (int g = 0; g < h->nstage; ++g) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[g], 0));
-    TL_TRY(h, cudaEventRecord(t.end, cs));
-    TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
-    t.nk = s.N;
-    t.depth = h->d;
-    t.launches = s.N + dx_launches;
-    t.reused = reused;
-    t.h2d_bytes = int64_t(s.N - reused) * int64_t(tb);
-    t.d2h_bytes = int64_t(s.N) * int64_t(tb);
-    end_call(h->bwd, t);
-    return TL_OK;
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return fail(h, TL_ERR_CUDA, "cudaSetDevice failed");
+    if ((st = finish_auto_depth(h)) != TL_OK) return st;
+    return backward_tiles(h, T, x_dev, y_dev, dy_dev, dx_dev, scr_dx, scr_dy, static_cast<cudaStream_t>(stream));
 }
 
 tl_status tiled_linear_destroy(tl_handle* h) {
@@ -977,7 +1183,7 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
     tl_stats* out = static_cast<tl_stats*>(out_v);
     std::memset(out, 0, sizeof(*out));
     DeviceGuard guard(h->device);
-    out->n_tiles = h->s.N;
+    out->n_tiles = h->n_total;
     out->depth = h->d;
     tl_status st = harvest_all(h, h->fwd);
     if (st == TL_OK) st = harvest_all(h, h->bwd);
@@ -998,8 +1204,8 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
         out->bwd_valid = 1;
         out->bwd_total_ms = c.total;
         out->bwd_gemm_ms = c.gemm1 + c.gemm2;
-        out->bwd_dw_gemm_ms = c.nk == h->s.N ? c.gemm1 : 0.f;
-        out->bwd_dx_gemm_ms = c.nk == h->s.N ? c.gemm2 : 0.f;
+        out->bwd_dw_gemm_ms = c.nk == h->n_total ? c.gemm1 : 0.f;
+        out->bwd_dx_gemm_ms = c.nk == h->n_total ? c.gemm2 : 0.f;
         out->bwd_h2d_ms = c.h2d;
         out->bwd_d2h_ms = c.d2h;
         out->bwd_wait_ms = c.total - c.gemm1 - c.gemm2;

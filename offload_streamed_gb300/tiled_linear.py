@@ -92,6 +92,16 @@ def load():
         L.tiled_linear_reset_stats.restype = st
         L.tiled_linear_set_tile_reuse.argtypes = [vp, i32]
         L.tiled_linear_set_tile_reuse.restype = st
+        L.tiled_linear_chain_workspace_bytes.argtypes = [i32, vp, vp, i32]
+        L.tiled_linear_chain_workspace_bytes.restype = sz
+        L.tiled_linear_chain_create.argtypes = [ctypes.POINTER(vp), i32, vp, vp, i32, vp, vp, vp, sz, ctypes.c_int]
+        L.tiled_linear_chain_create.restype = st
+        L.tiled_linear_chain_forward.argtypes = [vp, i64, vp, vp, vp]
+        L.tiled_linear_chain_forward.restype = st
+        L.tiled_linear_chain_scratch_bytes.argtypes = [i64, i32, vp]
+        L.tiled_linear_chain_scratch_bytes.restype = sz
+        L.tiled_linear_chain_backward.argtypes = [vp, i64, vp, vp, vp, vp, vp, sz, vp]
+        L.tiled_linear_chain_backward.restype = st
         L.tiled_linear_gemm_forward.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp]
         L.tiled_linear_gemm_forward.restype = st
         L.tiled_linear_gemm_dw.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp]
@@ -168,6 +178,46 @@ def tiled_linear_reset_stats(h: int) -> None:
 
 def tiled_linear_set_tile_reuse(h: int, enable: bool) -> None:
     _check(load().tiled_linear_set_tile_reuse(h, 1 if enable else 0), "tiled_linear_set_tile_reuse", h)
+
+
+def _i64s(v):
+    return (ctypes.c_int64 * len(v))(*[int(a) for a in v])
+
+
+def _i32s(v):
+    return (ctypes.c_int32 * len(v))(*[int(a) for a in v])
+
+
+def _ptrs(v):
+    return (ctypes.c_void_p * len(v))(*[int(a) if a else None for a in v])
+
+
+def tiled_linear_chain_workspace_bytes(L: int, dims, n_tiles, d: int) -> int:
+    return int(load().tiled_linear_chain_workspace_bytes(L, _i64s(dims), _i32s(n_tiles), d))
+
+
+def tiled_linear_chain_create(L, dims, n_tiles, d, w_hosts, dw_hosts, workspace_dev, workspace_bytes,
+                              device) -> int:
+    h = ctypes.c_void_p()
+    _check(load().tiled_linear_chain_create(ctypes.byref(h), L, _i64s(dims), _i32s(n_tiles), d,
+                                            _ptrs(w_hosts), _ptrs(dw_hosts), workspace_dev, workspace_bytes,
+                                            device), "tiled_linear_chain_create")
+    return h.value
+
+
+def tiled_linear_chain_forward(h: int, T: int, x_dev: int, y_devs, stream: int) -> None:
+    _check(load().tiled_linear_chain_forward(h, T, x_dev, _ptrs(y_devs), stream), "tiled_linear_chain_forward", h)
+
+
+def tiled_linear_chain_scratch_bytes(T: int, L: int, dims) -> int:
+    return int(load().tiled_linear_chain_scratch_bytes(T, L, _i64s(dims)))
+
+
+def tiled_linear_chain_backward(h: int, T: int, x_dev: int, y_devs, dy_dev: int, dx_dev: int, scratch_dev: int,
+                                scratch_bytes: int, stream: int) -> None:
+    _check(load().tiled_linear_chain_backward(h, T, x_dev, _ptrs(y_devs) if y_devs is not None else None, dy_dev,
+                                              dx_dev, scratch_dev, scratch_bytes, stream),
+           "tiled_linear_chain_backward", h)
 
 
 def tiled_linear_gemm_forward(T, K, n, x, ldx, w, ldw, y, ldy, err, stream) -> None:
@@ -304,6 +354,81 @@ class TiledLinear:
     def set_tile_reuse(self, enable: bool = True) -> None:
         """Let backward calls take the tiles still resident from the calls
         before them (W must not change in between)."""
+        tiled_linear_set_tile_reuse(self.handle, enable)
+
+    def close(self) -> int:
+        st = TL_OK
+        if self.handle:
+            st = tiled_linear_destroy(self.handle)
+            self.handle = 0
+        return st
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class TiledLinearChain:
+    """A chain of tiled linear operators (see the chain section of
+    ``include/tiled_linear.h``): operator l maps dims[l] -> dims[l+1] with its
+    W_l in n_tiles[l] column tiles, tile-major in pinned host memory.  One
+    ring and one prefetcher serve the whole chain."""
+
+    def __init__(self, dims, n_tiles, d: int, w_hosts, dw_hosts, device=None):
+        import torch
+        self.dims = [int(v) for v in dims]
+        self.n_tiles = [int(v) for v in n_tiles]
+        self.L = len(self.n_tiles)
+        if len(self.dims) != self.L + 1:
+            raise ValueError("dims needs one entry more than n_tiles")
+        self.d = int(d)
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
+                                   torch.device(device).index or 0)
+        wb = tiled_linear_chain_workspace_bytes(self.L, self.dims, self.n_tiles, self.d)
+        if wb == 0:
+            raise TiledLinearError(TL_ERR_INVALID, "tiled_linear_chain_workspace_bytes",
+                                   f"invalid chain dims={self.dims} n_tiles={self.n_tiles} d={d}")
+        self.workspace = torch.empty(wb, dtype=torch.uint8, device=self.device)
+        self._w, self._dw = list(w_hosts), list(dw_hosts)
+        ptr = lambda b: b.ptr if isinstance(b, PinnedBuffer) else b.data_ptr()
+        self.handle = tiled_linear_chain_create(self.L, self.dims, self.n_tiles, self.d,
+                                                [ptr(b) for b in self._w], [ptr(b) for b in self._dw],
+                                                self.workspace.data_ptr(), wb, self.device.index)
+        self._scratch = None
+
+    def forward(self, x, ys=None, stream=None):
+        """Returns the list of every operator's output (keep it for backward)."""
+        import torch
+        T = x.shape[0]
+        if ys is None:
+            ys = [torch.empty(T, self.dims[l + 1], dtype=torch.bfloat16, device=self.device)
+                  for l in range(self.L)]
+        tiled_linear_chain_forward(self.handle, T, x.data_ptr(), [y.data_ptr() for y in ys],
+                                   _stream_handle(stream))
+        return ys
+
+    def backward(self, x, ys, dy, dx=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if dx is None:
+            dx = torch.empty(T, self.dims[0], dtype=torch.float32, device=self.device)
+        need = tiled_linear_chain_scratch_bytes(T, self.L, self.dims)
+        if need and (self._scratch is None or self._scratch.numel() < need):
+            self._scratch = torch.empty(need, dtype=torch.uint8, device=self.device)
+        sp = self._scratch.data_ptr() if need else 0
+        tiled_linear_chain_backward(self.handle, T, x.data_ptr(), [y.data_ptr() for y in ys] if ys else None,
+                                    dy.data_ptr(), dx.data_ptr(), sp, need, _stream_handle(stream))
+        return dx
+
+    def stats(self) -> dict:
+        return tiled_linear_get_stats(self.handle)
+
+    def reset_stats(self) -> None:
+        tiled_linear_reset_stats(self.handle)
+
+    def set_tile_reuse(self, enable: bool = True) -> None:
         tiled_linear_set_tile_reuse(self.handle, enable)
 
     def close(self) -> int:

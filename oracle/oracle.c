@@ -26,6 +26,14 @@
  * only the additions round.  Outputs stay fp32 and are not rounded to bf16.
  * Build with -ffp-contract=off so that the result is identical on every host.
  *
+ * Chains of operators (Y_l = X_l.W_l, X_{l+1} = Y_l; with two operators, the
+ * FFN's two matrices, tm_zero_infinity, "Memory-centric tiling: operators
+ * bigger than the device") pass activations and gradients between the
+ * operators in bf16: X_{l+1} = bf16(Y_l) and, in the backward, the dY of
+ * operator l is bf16(dX of operator l+1).  oracle_round_bf16 is that
+ * rounding, round to nearest with ties to even; the chain itself is composed
+ * from the single-operator functions in oracle.py.
+ *
  * Layouts: row-major.  X [T,K] (ld K), W [K,M] (ld M), dY [T,M] (ld M),
  * Y [T,M], dX [T,K], dW [K,M].  The sampled functions also read W stored
  * tile by tile: M/C column blocks of C columns, block j held as its own
@@ -179,4 +187,27 @@ void oracle_sample_dw(int64_t T, int64_t K, int64_t M,
             acc = acc + bf16_to_f32(X[t * K + k]) * bf16_to_f32(dY[t * M + m]);
         out[i] = acc;
     }
+}
+
+/* bf16 keeps the sign, the 8 exponent bits and the top 7 fraction bits of an
+ * fp32 value.  Rounding to nearest, ties to even, on the bit pattern u: the
+ * dropped low 16 bits are compared with half (0x8000); adding 0x7FFF plus the
+ * lowest kept bit carries into the kept bits exactly when they exceed half,
+ * or equal it with an odd kept part.  A carry out of the fraction bumps the
+ * exponent, which is the correct next value (up to infinity).  NaN is kept
+ * NaN (quiet bit set) instead of being rounded. */
+static uint16_t f32_to_bf16_rne(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* out[i] = bf16 bits of in[i] rounded to nearest even, i < n. */
+void oracle_round_bf16(int64_t n, const float *in, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bf16_rne(in[i]);
 }

@@ -64,6 +64,8 @@ def load(path: str | None = None):
             fn.restype = None
         lib.oracle_sample_dw.argtypes = [i64, i64, i64, p, p, i64, p, p, p]
         lib.oracle_sample_dw.restype = None
+        lib.oracle_round_bf16.argtypes = [i64, p, p]
+        lib.oracle_round_bf16.restype = None
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         if path is None:
@@ -126,6 +128,47 @@ def backward_dw(X: np.ndarray, dY: np.ndarray, lib=None) -> np.ndarray:
 
 def backward(X, W, dY, lib=None):
     return backward_dx(dY, W, lib), backward_dw(X, dY, lib)
+
+
+def round_bf16(a: np.ndarray, lib=None) -> np.ndarray:
+    """bf16 bits (np.uint16) of the fp32 array ``a`` rounded to nearest, ties
+    to even (NaN stays NaN)."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    (lib or load()).oracle_round_bf16(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def chain_forward(X: np.ndarray, Ws, lib=None) -> list:
+    """Operators in sequence: Y_0 = X.W_0, Y_l = bf16(Y_{l-1}).W_l.  Returns the
+    fp32 Y_l of every operator (each from the bf16-rounded input before it)."""
+    ys, x = [], X
+    for W in Ws:
+        y = forward(x, W, lib)
+        ys.append(y)
+        x = round_bf16(y, lib)
+    return ys
+
+
+def chain_backward(X: np.ndarray, Ws, dY: np.ndarray, lib=None):
+    """Backward through chain_forward's operators, last to first: operator l
+    takes dY_l (dY for the last, bf16(dX_{l+1}) before it) and its input X_l
+    (X, then bf16(Y_{l-1})); dX_l = dY_l.W_l^T, dW_l = X_l^T.dY_l.  Returns
+    (dX_0 in fp32, [dW_0, ..., dW_{L-1}] in fp32)."""
+    xs, x = [], X
+    for W in Ws[:-1]:
+        xs.append(x)
+        x = round_bf16(forward(x, W, lib), lib)
+    xs.append(x)
+    dws = [None] * len(Ws)
+    dy = dY
+    dx = None
+    for l in range(len(Ws) - 1, -1, -1):
+        dx = backward_dx(dy, Ws[l], lib)
+        dws[l] = backward_dw(xs[l], dy, lib)
+        if l > 0:
+            dy = round_bf16(dx, lib)
+    return dx, dws
 
 
 def _idx(a) -> np.ndarray:

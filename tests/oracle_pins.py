@@ -15,7 +15,10 @@ the oracle disagrees with an independent fact:
   with one column block of W equals that block of the full product;
 * the adjoint identity <Y, dY> = <X, dX> = <W, dW> (all equal
   sum_{t,k,m} X[t,k] W[k,m] dY[t,m]);
-* sampled entries equal full-tensor entries, for both W storage layouts.
+* sampled entries equal full-tensor entries, for both W storage layouts;
+* fp32 -> bf16 rounding against torch's conversion and hand-made ties;
+* chains of two operators with one identity matrix, where the composition
+  reduces to single products and one rounding.
 
 Shapes are chosen with T, K, M pairwise distinct so that a transposed operand
 or a swapped index changes the answer.
@@ -189,5 +192,67 @@ def pin_sampled_brute_force(lib, seed=6, T=9, K=13, M=16, N=4):
         _check_close_exact(got[j], ex, s, T, f"sample_dw[{k},{m}]")
 
 
+def pin_round_bf16(lib):
+    """fp32 -> bf16 round-to-nearest-even against torch's conversion (an
+    independent library routine) for every sign / exponent / kept-fraction
+    pattern with the dropped half at and around the rounding boundaries, and
+    hand-made ties that must go to the even neighbour."""
+    import torch
+    hi = np.arange(65536, dtype=np.uint32) << np.uint32(16)
+    lows = np.array([0x0000, 0x0001, 0x7FFF, 0x8000, 0x8001, 0xFFFF], np.uint32)
+    f = (hi[:, None] | lows[None, :]).ravel().view(np.float32)
+    got = O.round_bf16(f, lib)
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(f)
+    assert np.array_equal(got[~nan], ref[~nan]), "round_bf16 differs from torch on finite / infinite values"
+    assert np.all(np.isnan(bf16_bits_to_f64(got[nan]))), "round_bf16 lost a NaN"
+    ties = {1 + 2.0 ** -8: 0x3F80, 1 + 3 * 2.0 ** -8: 0x3F82, -(1 + 2.0 ** -8): 0xBF80,
+            1 + 2.0 ** -8 + 2.0 ** -20: 0x3F81, 3.4028234663852886e38: 0x7F80, 2.0 ** -133: 0x0001,
+            2.0 ** -134: 0x0000, 3 * 2.0 ** -134: 0x0002}
+    got = O.round_bf16(np.array(list(ties), np.float32), lib)
+    assert list(got) == list(ties.values()), f"round_bf16 ties: {[hex(v) for v in got]}"
+
+
+def _eye_bits(n):
+    return f64_to_bf16_bits(np.eye(n))
+
+
+def pin_chain_identity_first(lib, seed=8, T=7, K=12, M=20):
+    """Chain (I, W1): the first operator passes X through exactly, so Y_1 is
+    the single product, dX_0 is the bf16 rounding of dX_1 (operator 1's dX)
+    and dW_0 = X^T.bf16(dX_1)."""
+    rng = np.random.default_rng(seed)
+    X = random_bf16(rng, (T, K))
+    W1 = random_bf16(rng, (K, M), 1 / np.sqrt(K))
+    dY = random_bf16(rng, (T, M))
+    ys = O.chain_forward(X, [_eye_bits(K), W1], lib)
+    assert np.array_equal(ys[0].astype(np.float64), bf16_bits_to_f64(X)), "chain (I, W): Y_0 != X"
+    assert np.array_equal(ys[1], O.forward(X, W1, lib)), "chain (I, W): Y_1 != X.W"
+    dx, dws = O.chain_backward(X, [_eye_bits(K), W1], dY, lib)
+    dx1 = O.backward_dx(dY, W1, lib)
+    dy0 = O.round_bf16(dx1, lib)
+    assert np.array_equal(dx.astype(np.float64), bf16_bits_to_f64(dy0)), "chain (I, W): dX_0 != bf16(dX_1)"
+    assert not np.array_equal(dx, dx1), "chain (I, W): the dY between operators was not rounded"
+    assert np.array_equal(dws[1], O.backward_dw(X, dY, lib)), "chain (I, W): dW_1"
+    assert np.array_equal(dws[0], O.backward_dw(X, dy0, lib)), "chain (I, W): dW_0"
+
+
+def pin_chain_identity_last(lib, seed=9, T=9, K=14, M=22):
+    """Chain (W0, I): Y_1 is the bf16 rounding of Y_0, dX_1 = dY exactly, so
+    dX_0 = dY.W0^T and dW_1 = bf16(Y_0)^T.dY."""
+    rng = np.random.default_rng(seed)
+    X = random_bf16(rng, (T, K))
+    W0 = random_bf16(rng, (K, M), 1 / np.sqrt(K))
+    dY = random_bf16(rng, (T, M))
+    ys = O.chain_forward(X, [W0, _eye_bits(M)], lib)
+    y0 = O.round_bf16(ys[0], lib)
+    assert np.array_equal(ys[1].astype(np.float64), bf16_bits_to_f64(y0)), "chain (W, I): Y_1 != bf16(Y_0)"
+    dx, dws = O.chain_backward(X, [W0, _eye_bits(M)], dY, lib)
+    assert np.array_equal(dx, O.backward_dx(dY, W0, lib)), "chain (W, I): dX_0 != dY.W0^T"
+    assert np.array_equal(dws[0], O.backward_dw(X, dY, lib)), "chain (W, I): dW_0"
+    assert np.array_equal(dws[1], O.backward_dw(y0, dY, lib)), "chain (W, I): dW_1"
+
+
 ALL_PINS = [pin_brute_force, pin_integer_exact, pin_identity, pin_concatenation,
-            pin_adjoint, pin_sampled, pin_sampled_brute_force]
+            pin_adjoint, pin_sampled, pin_sampled_brute_force, pin_round_bf16,
+            pin_chain_identity_first, pin_chain_identity_last]

@@ -133,3 +133,38 @@ def test_stats_struct_layout_matches_the_header(tl, tmp_path):
     out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     assert out[0] == ctypes.sizeof(tl.tl_stats)
     assert out[1:] == [getattr(tl.tl_stats, f).offset for f in fields]
+
+
+def test_chain_workspace_and_scratch_bytes(tl):
+    """Ring slots are sized for the chain's largest tile; d counts tiles over
+    all operators; one operator gives the single-operator figure."""
+    mib = 1 << 20
+    # GPT-scale FFN: up 8192 -> 32768 and down 32768 -> 8192, 8 tiles each (64 MiB tiles)
+    assert tl.tiled_linear_chain_workspace_bytes(2, [8192, 32768, 8192], [8, 8], 2) == HEADER + (3 + 2) * 64 * mib
+    # tiles of 2 MiB and 4 MiB: five tiles, d = 1 -> 2 ring slots + 2 staging slots of 4 MiB
+    assert tl.tiled_linear_chain_workspace_bytes(2, [1024, 4096, 512], [4, 1], 1) == HEADER + 4 * 4 * mib
+    for K, M, N, d in [(1024, 4096, 4, 1), (512, 1536, 3, -1), (264, 1200, 3, 0)]:
+        assert tl.tiled_linear_chain_workspace_bytes(1, [K, M], [N], d) == tl.tiled_linear_workspace_bytes(K, M, N, d)
+    assert tl.tiled_linear_chain_workspace_bytes(2, [1024, 4096, 500], [4, 3], 1) == 0  # 500 % 3
+    assert tl.tiled_linear_chain_workspace_bytes(0, [1024], [], 1) == 0
+    assert tl.tiled_linear_chain_scratch_bytes(100, 3, [64, 256, 128, 64]) == 100 * 256 * 4 + 100 * 256 * 2
+    assert tl.tiled_linear_chain_scratch_bytes(100, 1, [64, 256]) == 0
+
+
+def test_chain_create_argument_checks(tl):
+    lib = tl.load()
+    h = ctypes.c_void_p()
+    dims = (ctypes.c_int64 * 3)(256, 512, 256)
+    n = (ctypes.c_int32 * 2)(2, 2)
+    ptrs = (ctypes.c_void_p * 2)(16, 16)
+    # mismatched operator count / null arrays / bad shapes are refused before any CUDA call
+    assert lib.tiled_linear_chain_create(ctypes.byref(h), 0, dims, n, 1, ptrs, ptrs, 256, 1 << 30, 0) == \
+        tl.TL_ERR_INVALID
+    assert lib.tiled_linear_chain_create(ctypes.byref(h), 2, dims, n, 1, None, ptrs, 256, 1 << 30, 0) == \
+        tl.TL_ERR_INVALID
+    bad = (ctypes.c_int32 * 2)(3, 2)  # 512 % 3
+    assert lib.tiled_linear_chain_create(ctypes.byref(h), 2, dims, bad, 1, ptrs, ptrs, 256, 1 << 30, 0) == \
+        tl.TL_ERR_INVALID
+    assert h.value is None
+    assert lib.tiled_linear_chain_forward(None, 1, None, None, None) == tl.TL_ERR_STATE
+    assert lib.tiled_linear_chain_backward(None, 1, None, None, None, None, None, 0, None) == tl.TL_ERR_STATE

@@ -44,6 +44,12 @@ MUTANTS = {
     "sample_y_transposed_x": (
         "acc = acc + bf16_to_f32(X[t * K + k]) * bf16_to_f32(w_at(W, K, wcols, k, m));",
         "acc = acc + bf16_to_f32(X[(k % T) * K + (t % K)]) * bf16_to_f32(w_at(W, K, wcols, k, m));"),
+    "round_half_up": (
+        "u += 0x7FFFu + ((u >> 16) & 1u);",
+        "u += 0x8000u;"),
+    "round_truncates": (
+        "u += 0x7FFFu + ((u >> 16) & 1u);",
+        "u += 0u;"),
     "bf16_widening_shift": (
         "uint32_t u = ((uint32_t)h) << 16;",
         "uint32_t u = ((uint32_t)h) << 15;"),
