@@ -466,6 +466,41 @@ def profile_gemms(cfg, reps: int) -> None:
     log(f"[bench] profile-gemms: {reps} x (fwd, dW, dX over {nx} columns) at T={T} K={K} Mi={Mi}")
 
 
+def run_host_adam(tl, op, x, y, dy, dx, steps: int, dist: Dist, flops_step: float) -> dict:
+    """Forward + backward + the Adam step on the host CPU (fp32 master and
+    moments, all host threads), the update of each tile overlapping the GPU's
+    backward of the later ones.  Restores the host W afterwards."""
+    import torch
+    w_save = op._w.tensor.clone()
+    opt = tl.HostAdam(op, lr=1e-4, threads=0)
+    s = torch.cuda.current_stream()
+    for _ in range(2):
+        op.forward(x, y, stream=s)
+        op.backward(x, dy, dx, stream=s)
+        opt.step()
+    opt.wait()
+    torch.cuda.synchronize()
+    busy0 = opt.stats()["busy_seconds"]
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        op.forward(x, y, stream=s)
+        op.backward(x, dy, dx, stream=s)
+        opt.step()
+    opt.wait()
+    torch.cuda.synchronize()
+    ms = dist.max((time.perf_counter() - t0) * 1e3 / steps)
+    busy = (opt.stats()["busy_seconds"] - busy0) / steps
+    n = op._w.numel
+    opt.close()
+    op._w.tensor.copy_(w_save)
+    return {"value": round(dist.world * flops_step / (ms / 1e3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "steps": steps, "optimizer_busy_ms_per_step": round(busy * 1e3, 3),
+            "params": n, "host_optimizer_gbs": round(28.0 * n / busy / 1e9, 1) if busy > 0 else None,
+            "host_threads": os.cpu_count(),
+            "what": "forward + backward + Adam on the host CPU (fp32 master, m, v; 28 B per parameter read "
+                    "and written), each tile's update overlapping the GPU; host wall-clock per step"}
+
+
 def run_ffn_chain(tl, cfg, x, y_up, dx, seed: int, steps: int, dist: Dist) -> dict:
     """The workload's layer followed by its down-projection (M -> K, N tiles of
     K/N columns, W2 [M, K] pinned, tile-major), run as one chain: one ring and
@@ -695,6 +730,10 @@ def run_ours(args, cfg, dist: Dist):
             "h2d_bytes_per_step": rs["fwd_h2d_bytes"] + rs["bwd_h2d_bytes"],
             "what": "backward reuses the tiles still resident from forward (not the pages' method, which "
                     "refetches every tile; W unchanged between the two calls)"}
+
+    # --- training step with the Adam update on the host CPU (overlapped) -------
+    if not args.skip_aux and not persistent:
+        out["host_adam"] = run_host_adam(tl, op, x, y, dy, dx, max(3, min(args.steps, 10)), dist, flops_step)
 
     # --- the FFN chain (up- then down-projection) through one prefetcher -------
     if not args.skip_aux and not persistent and M % K == 0:

@@ -185,6 +185,72 @@ tl_status tiled_linear_reset_stats(tl_handle *h);
  * handle. */
 tl_status tiled_linear_set_tile_reuse(tl_handle *h, int32_t enable);
 
+/* --- the optimizer step on the host ----------------------------------------
+ * The Adam update runs on the CPU, beside the DRAM holding its state: it is
+ * elementwise, about 12 FLOPs against ~24 bytes read and written per
+ * parameter, so no host link could hide it behind GPU compute
+ * (tm_zero_infinity, "Applying the test: which state can live where").  The
+ * state is 12 bytes per parameter: fp32 master weight, first and second
+ * moment (gpu_zero_sharding, "The architecture: every piece explained").
+ * The update is Adam with bias correction and decoupled weight decay, in
+ * fp32, one element at a time:
+ *     g  = grad (+ the fp32 accumulator, when gradients were accumulated)
+ *     m  = beta1 m + (1 - beta1) g
+ *     v  = beta2 v + (1 - beta2) g^2
+ *     p  = p - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+ *            - lr weight_decay p
+ *     w  = bf16 round-to-nearest-even of p (the weights the next pass streams)
+ * The pages name Adam and its state but write no formula; this is the
+ * textbook update.  No part of it runs on the GPU. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    int32_t threads;  /* host threads of the optimizer below (<= 0: all) */
+} tl_adam_config;
+
+/* One Adam step (t = step >= 1) over n parameters, in the calling thread:
+ * master, m, v fp32 (updated), grad_bf16 the gradient (bf16 bits), grad_acc
+ * an fp32 gradient added to it (or NULL), w_bf16 receives the new weights.
+ * Errors: TL_ERR_INVALID (null pointers, bad config). */
+tl_status tiled_linear_adam_update(const tl_adam_config *cfg, int64_t step, int64_t n, float *master,
+                                   float *m, float *v, const float *grad_acc, const void *grad_bf16,
+                                   void *w_bf16);
+
+/* A host optimizer attached to a handle (per-tile launch mode; single
+ * operator or chain).  Per operator l: master[l], m[l], v[l] (and grad_acc[l]
+ * if grad_acc is not NULL) are fp32 host arrays of dims K x M elements, in
+ * the same layout as that operator's host W (row-major or tile-major); the
+ * caller owns them and initialises master (normally to W) and zeroes m, v.
+ * After a backward call:
+ *   tiled_linear_optimizer_accumulate: grad_acc (+)= that backward's dW (the
+ *     first accumulation after a step overwrites);
+ *   tiled_linear_optimizer_step: the Adam step with g = dW (+ grad_acc if it
+ *     was filled since the last step), writing master, m, v and the bf16 W in
+ *     the handle's host W buffer.
+ * Both return at once.  A worker thread takes the tiles in the backward's
+ * order as each one's dW lands in host memory, so the update overlaps the
+ * GPU's backward of the later tiles.  The handle's later calls wait (on the
+ * host) before queuing a copy of a tile's W until its update is done, and
+ * before writing a tile's dW until the worker has read the previous one:
+ * forward / backward may therefore block the calling thread.  Results are
+ * bit-identical to calling tiled_linear_adam_update tile by tile after the
+ * backward completes.  Host waits give up after 600 s with TL_ERR_TIMEOUT.
+ * Errors: TL_ERR_INVALID (arguments, persistent mode, accumulate without an
+ * accumulator), TL_ERR_STATE (no backward since the last optimizer call, or
+ * an optimizer already attached), TL_ERR_CUDA, TL_ERR_TIMEOUT. */
+typedef struct tl_optimizer tl_optimizer;
+tl_status tiled_linear_optimizer_create(tl_optimizer **out, tl_handle *h, const tl_adam_config *cfg,
+                                        float *const *master, float *const *m, float *const *v,
+                                        float *const *grad_acc);
+tl_status tiled_linear_optimizer_accumulate(tl_optimizer *o);
+tl_status tiled_linear_optimizer_step(tl_optimizer *o);
+/* Block until every submitted accumulation and step is done. */
+tl_status tiled_linear_optimizer_wait(tl_optimizer *o);
+/* Steps submitted so far, and host seconds spent updating. */
+tl_status tiled_linear_optimizer_stats(const tl_optimizer *o, int64_t *steps, double *busy_seconds);
+/* Wait for the submitted work, detach from the handle, free.  Destroy the
+ * optimizer before its handle (tiled_linear_destroy detaches it too). */
+tl_status tiled_linear_optimizer_destroy(tl_optimizer *o);
+
 /* --- chains of operators: one prefetcher across several linear layers -----
  * A chain of L tiled linear operators, run in sequence by one handle:
  * operator l computes Y_l [T, dims[l+1]] = X_l [T, dims[l]] . W_l with W_l

@@ -22,9 +22,12 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libtiled_linear.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# host code: no fused multiply-add contraction, so that the host-side
+# optimizer update gives the same bits on every host architecture
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-              "-I", INCLUDE, "-I", CSRC]
-UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_cast.cu"]
+              "-Xcompiler", "-ffp-contract=off", "-I", INCLUDE, "-I", CSRC]
+UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_cast.cu", "tl_adam.cpp",
+         "tl_optimizer.cpp"]
 
 
 def nvcc() -> str:
@@ -56,7 +59,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     cc = nvcc()
     objs, procs = [], []
     for u in UNITS:
-        obj = os.path.join(LIBDIR, u.replace(".cu", f".{os.getpid()}.o"))
+        obj = os.path.join(LIBDIR, f"{os.path.splitext(u)[0]}.{os.getpid()}.o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, u), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)

@@ -23,6 +23,7 @@
 #include "tiled_linear.h"
 #include "tl_cast.h"
 #include "tl_gemm.h"
+#include "tl_optimizer.h"
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -190,6 +191,14 @@ struct tl_handle {
     std::deque<int> slot_q;
     std::vector<int32_t> slot_tile;
     bool reuse = false;
+    // Host optimizer attached by tiled_linear_optimizer_create: its worker,
+    // per-tile events the backward records (W read by the GPU, dW in host
+    // memory) and the tile order of the last backward.
+    tl::Optimizer* opt = nullptr;
+    tl_optimizer* opt_owner = nullptr;  // the C object; its handle pointer is cleared on destroy
+    std::vector<cudaEvent_t> opt_ev_w, opt_ev_dw;
+    std::vector<int> opt_order;
+    bool opt_have_bwd = false;  // a backward recorded the events since the last submit
     int num_sms = 0;
     bool persistent = false;  // whole passes as one persistent launch
     uint32_t* flags = nullptr;
@@ -396,6 +405,19 @@ int take_slot(tl_handle* h) {
     const int sl = h->slot_q.front();
     h->slot_q.pop_front();
     return sl;
+}
+
+// With a host optimizer attached: the host waits before it queues a copy that
+// reads tile g's W (until every submitted step has rewritten it) or writes
+// tile g's dW (until every submitted job has read the last one).
+constexpr double kOptWaitSeconds = 600.0;
+
+tl_status opt_wait(tl_handle* h, int g, bool update) {
+    if (!h->opt) return TL_OK;
+    const bool ok = update ? tl::optimizer_wait_update(h->opt, g, kOptWaitSeconds)
+                           : tl::optimizer_wait_read(h->opt, g, kOptWaitSeconds);
+    if (!ok) return fail(h, TL_ERR_TIMEOUT, tl::optimizer_error(h->opt));
+    return TL_OK;
 }
 
 // Automatic depth: after the first forward call, d = ceil(t_fetch / t_layer)
@@ -761,6 +783,7 @@ tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys,
         const void* xl = l == 0 ? x : ys[l - 1];
         for (int i = 0; i < s.N; ++i) {
             const int g = o.first + i;  // tile index in the handle's order
+            if ((st = opt_wait(h, g, true)) != TL_OK) return st;
             const int sl = take_slot(h);
             if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
             h->slot_tile[size_t(sl)] = -1;
@@ -815,12 +838,24 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
     tl_status st;
     const int L = int(h->ops.size());
     if (T == 0) {  // dW = X^T dY over an empty sum: zero
-        for (const Op& o : h->ops) {
+        if (h->opt) h->opt_order.clear();
+        for (int l = L - 1; l >= 0; --l) {
+            const Op& o = h->ops[size_t(l)];
             TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[0], 0));
             TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tile_bytes(o.s.K, o.s.Mi), cs));
-            for (int i = 0; i < o.s.N; ++i) TL_TRY(h, copy_dw_tile(o, i, h->stage[0], cs));
+            for (int i = o.s.N - 1; i >= 0; --i) {
+                const int g = o.first + i;
+                if ((st = opt_wait(h, g, false)) != TL_OK) return st;
+                TL_TRY(h, copy_dw_tile(o, i, h->stage[0], cs));
+                if (h->opt) {
+                    TL_TRY(h, cudaEventRecord(h->opt_ev_w[size_t(g)], cs));
+                    TL_TRY(h, cudaEventRecord(h->opt_ev_dw[size_t(g)], cs));
+                    h->opt_order.push_back(g);
+                }
+            }
             TL_TRY(h, cudaEventRecord(h->ev_drained[0], cs));
         }
+        if (h->opt) h->opt_have_bwd = true;
         return TL_OK;
     }
     CallSlot* tp = begin_call(h, h->bwd, &st);
@@ -847,6 +882,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
     int64_t h2d_bytes = 0, d2h_bytes = 0;
     int launches = 0;
     int jg = 0;  // position in the backward's tile order
+    if (h->opt) h->opt_order.clear();
     TL_TRY(h, cudaEventRecord(t.start, cs));
     for (int l = L - 1; l >= 0; --l) {
         const Op& o = h->ops[size_t(l)];
@@ -871,6 +907,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
                 TL_TRY(h, cudaEventRecord(t.ev[4][jg], h->h2d));
                 TL_TRY(h, cudaEventRecord(t.ev[5][jg], h->h2d));
             } else {  // refetch W_i
+                if ((st = opt_wait(h, g, true)) != TL_OK) return st;
                 sl = take_slot(h);
                 if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
                 h->slot_tile[size_t(sl)] = -1;
@@ -882,6 +919,9 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
                 h->slot_tile[size_t(sl)] = g;
                 h2d_bytes += int64_t(tb);
             }
+            // the host W of tile g is no longer read by this call once the
+            // h2d stream gets here
+            if (h->opt) TL_TRY(h, cudaEventRecord(h->opt_ev_w[size_t(g)], h->h2d));
 
             // dW_i = X^T dY_i into staging slot gs (does not need W_i)
             TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gs], 0));
@@ -906,10 +946,15 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             TL_TRY(h, cudaEventRecord(h->ev_dwdone[gs], cs));
 
             // write dW_i back on the d2h stream
+            if ((st = opt_wait(h, g, false)) != TL_OK) return st;
             TL_TRY(h, cudaStreamWaitEvent(h->d2h, h->ev_dwdone[gs], 0));
             TL_TRY(h, cudaEventRecord(t.ev[6][jg], h->d2h));
             TL_TRY(h, copy_dw_tile(o, i, h->stage[gs], h->d2h));
             TL_TRY(h, cudaEventRecord(t.ev[7][jg], h->d2h));
+            if (h->opt) {
+                TL_TRY(h, cudaEventRecord(h->opt_ev_dw[size_t(g)], h->d2h));
+                h->opt_order.push_back(g);
+            }
             TL_TRY(h, cudaEventRecord(h->ev_drained[gs], h->d2h));
             d2h_bytes += int64_t(tb);
 
@@ -966,6 +1011,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
     for (int gi = 0; gi < h->nstage; ++gi) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gi], 0));
     TL_TRY(h, cudaEventRecord(t.end, cs));
     TL_TRY(h, cudaMemcpyAsync(h->err_mirror, h->err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    if (h->opt) h->opt_have_bwd = true;
     t.nk = NT;
     t.depth = h->d;
     t.launches = launches;
@@ -1143,11 +1189,33 @@ tl_status tiled_linear_chain_backward(tl_handle* h, int64_t T, const void* x_dev
     return backward_tiles(h, T, x_dev, y_dev, dy_dev, dx_dev, scr_dx, scr_dy, static_cast<cudaStream_t>(stream));
 }
 
+struct tl_optimizer {
+    tl_handle* h = nullptr;
+    bool has_acc = false;
+};
+
+static void detach_optimizer(tl_handle* h) {
+    if (h->opt_owner) {
+        h->opt_owner->h = nullptr;
+        h->opt_owner = nullptr;
+    }
+    if (!h->opt) return;
+    tl::optimizer_delete(h->opt);  // waits for the submitted jobs
+    h->opt = nullptr;
+    for (auto* v : {&h->opt_ev_w, &h->opt_ev_dw}) {
+        for (auto e : *v)
+            if (e) cudaEventDestroy(e);
+        v->clear();
+    }
+    h->opt_have_bwd = false;
+}
+
 tl_status tiled_linear_destroy(tl_handle* h) {
     if (!h) return TL_OK;
     tl_status st = h->sticky;
     {
         DeviceGuard guard(h->device);
+        detach_optimizer(h);
         if (h->h2d) cudaStreamSynchronize(h->h2d);
         if (h->d2h) cudaStreamSynchronize(h->d2h);
         for (auto* v : {&h->ev_ready, &h->ev_free, &h->ev_dwdone, &h->ev_drained})
@@ -1232,6 +1300,148 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
         return fail(h, TL_ERR_TIMEOUT,
                     "a kernel's bounded wait timed out (error bits " + std::to_string(word) + ")");
     return h->sticky;
+}
+
+static std::string adam_config_error(const tl_adam_config* c) {
+    if (!c) return "null config";
+    if (!(c->lr >= 0.f) || !std::isfinite(c->lr)) return "lr must be finite and >= 0";
+    if (!(c->beta1 >= 0.f && c->beta1 < 1.f) || !(c->beta2 >= 0.f && c->beta2 < 1.f))
+        return "beta1 and beta2 must be in [0, 1)";
+    if (!(c->eps > 0.f) || !std::isfinite(c->eps)) return "eps must be finite and > 0";
+    if (!(c->weight_decay >= 0.f) || !std::isfinite(c->weight_decay)) return "weight_decay must be finite and >= 0";
+    return {};
+}
+
+static tl::AdamHyper hyper(const tl_adam_config* c) {
+    tl::AdamHyper hp;
+    hp.lr = c->lr;
+    hp.beta1 = c->beta1;
+    hp.beta2 = c->beta2;
+    hp.eps = c->eps;
+    hp.weight_decay = c->weight_decay;
+    return hp;
+}
+
+tl_status tiled_linear_adam_update(const tl_adam_config* cfg, int64_t step, int64_t n, float* master, float* m,
+                                   float* v, const float* grad_acc, const void* grad_bf16, void* w_bf16) {
+    if (!adam_config_error(cfg).empty() || step < 1 || n < 0) return TL_ERR_INVALID;
+    if (n == 0) return TL_OK;
+    if (!master || !m || !v || !grad_bf16 || !w_bf16) return TL_ERR_INVALID;
+    tl::Block b;
+    b.master = master;
+    b.m = m;
+    b.v = v;
+    b.acc = const_cast<float*>(grad_acc);
+    b.grad = static_cast<const uint16_t*>(grad_bf16);
+    b.w = static_cast<uint16_t*>(w_bf16);
+    b.rows = 1;
+    b.cols = n;
+    b.ld = n;
+    tl::adam_rows(b, hyper(cfg), step, grad_acc != nullptr, 0, 1);
+    return TL_OK;
+}
+
+tl_status tiled_linear_optimizer_create(tl_optimizer** out, tl_handle* h, const tl_adam_config* cfg,
+                                        float* const* master, float* const* m, float* const* v,
+                                        float* const* grad_acc) {
+    if (!out) return TL_ERR_INVALID;
+    *out = nullptr;
+    tl_status st = check_usable(h);
+    if (st != TL_OK) return st;
+    const std::string bad = adam_config_error(cfg);
+    if (!bad.empty()) return fail(h, TL_ERR_INVALID, "optimizer config: " + bad);
+    if (h->persistent) return fail(h, TL_ERR_INVALID, "the host optimizer needs the per-tile launch mode");
+    if (h->opt) return fail(h, TL_ERR_STATE, "the handle already has an optimizer");
+    if (!master || !m || !v) return fail(h, TL_ERR_INVALID, "null master, m or v array");
+    std::vector<tl::Block> tiles;
+    for (size_t l = 0; l < h->ops.size(); ++l) {
+        const Op& o = h->ops[l];
+        if (!master[l] || !m[l] || !v[l] || (grad_acc && !grad_acc[l]))
+            return fail(h, TL_ERR_INVALID, "null parameter array for operator " + std::to_string(l));
+        for (int i = 0; i < o.s.N; ++i) {
+            const bool tm = o.layout == TL_LAYOUT_TILE_MAJOR;
+            const size_t off = tm ? size_t(i) * size_t(o.s.K) * size_t(o.s.Mi) : size_t(i) * size_t(o.s.Mi);
+            tl::Block b;
+            b.master = master[l] + off;
+            b.m = m[l] + off;
+            b.v = v[l] + off;
+            b.acc = grad_acc ? grad_acc[l] + off : nullptr;
+            b.grad = reinterpret_cast<const uint16_t*>(o.dw_host) + off;
+            b.w = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(o.w_host)) + off;
+            b.rows = o.s.K;
+            b.cols = o.s.Mi;
+            b.ld = tm ? o.s.Mi : o.s.M;
+            tiles.push_back(b);
+        }
+    }
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return fail(h, TL_ERR_CUDA, "cudaSetDevice failed");
+    auto* o = new (std::nothrow) tl_optimizer();
+    if (!o) return fail(h, TL_ERR_INVALID, "out of host memory");
+    h->opt_ev_w.assign(size_t(h->n_total), nullptr);
+    h->opt_ev_dw.assign(size_t(h->n_total), nullptr);
+    for (auto* vv : {&h->opt_ev_w, &h->opt_ev_dw})
+        for (auto& e : *vv)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+                detach_optimizer(h);
+                delete o;
+                return fail(h, TL_ERR_CUDA, "optimizer event creation failed");
+            }
+    try {
+        h->opt = tl::optimizer_new(tiles, hyper(cfg), cfg->threads);
+    } catch (const std::exception& e) {
+        detach_optimizer(h);
+        delete o;
+        return fail(h, TL_ERR_INVALID, std::string("optimizer threads: ") + e.what());
+    }
+    h->opt_have_bwd = false;
+    h->opt_owner = o;
+    o->h = h;
+    o->has_acc = grad_acc != nullptr;
+    *out = o;
+    return TL_OK;
+}
+
+static tl_status optimizer_submit_job(tl_optimizer* o, bool step) {
+    if (!o || !o->h || !o->h->opt) return TL_ERR_STATE;
+    tl_handle* h = o->h;
+    tl_status st = check_usable(h);
+    if (st != TL_OK) return st;
+    if (!step && !o->has_acc) return fail(h, TL_ERR_INVALID, "accumulate needs a gradient accumulator");
+    if (!h->opt_have_bwd) return fail(h, TL_ERR_STATE, "no backward since the last optimizer call");
+    if (!tl::optimizer_submit(h->opt, step, h->opt_order, h->opt_ev_w, h->opt_ev_dw))
+        return fail(h, TL_ERR_TIMEOUT, tl::optimizer_error(h->opt));
+    h->opt_have_bwd = false;
+    return TL_OK;
+}
+
+tl_status tiled_linear_optimizer_accumulate(tl_optimizer* o) { return optimizer_submit_job(o, false); }
+tl_status tiled_linear_optimizer_step(tl_optimizer* o) { return optimizer_submit_job(o, true); }
+
+tl_status tiled_linear_optimizer_wait(tl_optimizer* o) {
+    if (!o || !o->h || !o->h->opt) return TL_ERR_STATE;
+    if (!tl::optimizer_wait_all(o->h->opt, kOptWaitSeconds))
+        return fail(o->h, TL_ERR_TIMEOUT, tl::optimizer_error(o->h->opt));
+    return TL_OK;
+}
+
+tl_status tiled_linear_optimizer_stats(const tl_optimizer* o, int64_t* steps, double* busy_seconds) {
+    if (!o || !o->h || !o->h->opt) return TL_ERR_STATE;
+    if (steps) *steps = tl::optimizer_steps(o->h->opt);
+    if (busy_seconds) *busy_seconds = tl::optimizer_busy_seconds(o->h->opt);
+    return TL_OK;
+}
+
+tl_status tiled_linear_optimizer_destroy(tl_optimizer* o) {
+    if (!o) return TL_OK;
+    tl_status st = TL_OK;
+    if (o->h && o->h->opt) {
+        if (!tl::optimizer_error(o->h->opt).empty()) st = TL_ERR_TIMEOUT;
+        DeviceGuard guard(o->h->device);
+        detach_optimizer(o->h);
+    }
+    delete o;
+    return st;
 }
 
 tl_status tiled_linear_set_tile_reuse(tl_handle* h, int32_t enable) {

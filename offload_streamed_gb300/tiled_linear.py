@@ -51,6 +51,11 @@ class tl_stats(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class tl_adam_config(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("threads", ctypes.c_int32)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -92,6 +97,16 @@ def load():
         L.tiled_linear_reset_stats.restype = st
         L.tiled_linear_set_tile_reuse.argtypes = [vp, i32]
         L.tiled_linear_set_tile_reuse.restype = st
+        L.tiled_linear_adam_update.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, vp]
+        L.tiled_linear_adam_update.restype = st
+        L.tiled_linear_optimizer_create.argtypes = [ctypes.POINTER(vp), vp, vp, vp, vp, vp, vp]
+        L.tiled_linear_optimizer_create.restype = st
+        for name in ("tiled_linear_optimizer_accumulate", "tiled_linear_optimizer_step",
+                     "tiled_linear_optimizer_wait", "tiled_linear_optimizer_destroy"):
+            getattr(L, name).argtypes = [vp]
+            getattr(L, name).restype = st
+        L.tiled_linear_optimizer_stats.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
+        L.tiled_linear_optimizer_stats.restype = st
         L.tiled_linear_chain_workspace_bytes.argtypes = [i32, vp, vp, i32]
         L.tiled_linear_chain_workspace_bytes.restype = sz
         L.tiled_linear_chain_create.argtypes = [ctypes.POINTER(vp), i32, vp, vp, i32, vp, vp, vp, sz, ctypes.c_int]
@@ -218,6 +233,47 @@ def tiled_linear_chain_backward(h: int, T: int, x_dev: int, y_devs, dy_dev: int,
     _check(load().tiled_linear_chain_backward(h, T, x_dev, _ptrs(y_devs) if y_devs is not None else None, dy_dev,
                                               dx_dev, scratch_dev, scratch_bytes, stream),
            "tiled_linear_chain_backward", h)
+
+
+def adam_config(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, threads=0) -> tl_adam_config:
+    return tl_adam_config(lr, beta1, beta2, eps, weight_decay, threads)
+
+
+def tiled_linear_adam_update(cfg: tl_adam_config, step: int, n: int, master: int, m: int, v: int, grad_acc: int,
+                             grad_bf16: int, w_bf16: int) -> None:
+    _check(load().tiled_linear_adam_update(ctypes.byref(cfg), step, n, master, m, v, grad_acc or None, grad_bf16,
+                                           w_bf16), "tiled_linear_adam_update")
+
+
+def tiled_linear_optimizer_create(h: int, cfg: tl_adam_config, masters, ms, vs, accs=None) -> int:
+    o = ctypes.c_void_p()
+    _check(load().tiled_linear_optimizer_create(ctypes.byref(o), h, ctypes.byref(cfg), _ptrs(masters), _ptrs(ms),
+                                                _ptrs(vs), _ptrs(accs) if accs else None),
+           "tiled_linear_optimizer_create", h)
+    return o.value
+
+
+def tiled_linear_optimizer_accumulate(o: int, h=None) -> None:
+    _check(load().tiled_linear_optimizer_accumulate(o), "tiled_linear_optimizer_accumulate", h)
+
+
+def tiled_linear_optimizer_step(o: int, h=None) -> None:
+    _check(load().tiled_linear_optimizer_step(o), "tiled_linear_optimizer_step", h)
+
+
+def tiled_linear_optimizer_wait(o: int, h=None) -> None:
+    _check(load().tiled_linear_optimizer_wait(o), "tiled_linear_optimizer_wait", h)
+
+
+def tiled_linear_optimizer_stats(o: int) -> tuple:
+    steps, busy = ctypes.c_int64(), ctypes.c_double()
+    _check(load().tiled_linear_optimizer_stats(o, ctypes.byref(steps), ctypes.byref(busy)),
+           "tiled_linear_optimizer_stats")
+    return steps.value, busy.value
+
+
+def tiled_linear_optimizer_destroy(o: int) -> int:
+    return int(load().tiled_linear_optimizer_destroy(o))
 
 
 def tiled_linear_gemm_forward(T, K, n, x, ldx, w, ldw, y, ldy, err, stream) -> None:
@@ -435,6 +491,57 @@ class TiledLinearChain:
         st = TL_OK
         if self.handle:
             st = tiled_linear_destroy(self.handle)
+            self.handle = 0
+        return st
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class HostAdam:
+    """The Adam step on the host CPU for a ``TiledLinear`` or
+    ``TiledLinearChain`` (see the optimizer section of
+    ``include/tiled_linear.h``).  Keeps fp32 master weights (initialised from
+    the op's host W), first and second moments, and optionally an fp32
+    gradient accumulator, in the layout of each operator's host W.  After a
+    backward call, ``step()`` (or ``accumulate()``) returns at once; the update
+    overlaps the GPU, and the op's next calls wait for the tiles they read."""
+
+    def __init__(self, op, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, threads=0,
+                 accumulate=False):
+        import torch
+        self.op = op
+        ws = op._w if isinstance(op._w, list) else [op._w]
+        hosts = [b.tensor if isinstance(b, PinnedBuffer) else b for b in ws]
+        self.master = [h.view(-1).float() for h in hosts]
+        self.m = [torch.zeros_like(a) for a in self.master]
+        self.v = [torch.zeros_like(a) for a in self.master]
+        self.acc = [torch.zeros_like(a) for a in self.master] if accumulate else None
+        self.cfg = adam_config(lr, beta1, beta2, eps, weight_decay, threads)
+        ptr = lambda ts: [t.data_ptr() for t in ts]
+        self.handle = tiled_linear_optimizer_create(op.handle, self.cfg, ptr(self.master), ptr(self.m), ptr(self.v),
+                                                    ptr(self.acc) if self.acc else None)
+
+    def step(self) -> None:
+        tiled_linear_optimizer_step(self.handle, self.op.handle)
+
+    def accumulate(self) -> None:
+        tiled_linear_optimizer_accumulate(self.handle, self.op.handle)
+
+    def wait(self) -> None:
+        tiled_linear_optimizer_wait(self.handle, self.op.handle)
+
+    def stats(self) -> dict:
+        steps, busy = tiled_linear_optimizer_stats(self.handle)
+        return {"steps": steps, "busy_seconds": busy}
+
+    def close(self) -> int:
+        st = TL_OK
+        if self.handle:
+            st = tiled_linear_optimizer_destroy(self.handle)
             self.handle = 0
         return st
 
