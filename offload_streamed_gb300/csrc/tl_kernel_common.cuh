@@ -164,12 +164,16 @@ __device__ __forceinline__ void epi_bf16_tma(const CUtensorMap* map, uint32_t t_
 // added and stored.
 __device__ __forceinline__ void epi_f32_direct(float* out_row, bool row_ok, int rem0, uint32_t t_row, int nchunks,
                                                bool rmw) {
+    // The output streams through L2 once per launch (read and written back):
+    // evict it first, so that it does not push out the operand blocks the
+    // tile order keeps resident.
+    const uint64_t pol = l2_policy_evict_first();
     auto load_old = [&](int c, float4(&dst)[8]) {
         const float* src = out_row + c * 32;
         const int rem = rem0 - c * 32;
         if (row_ok && rem >= 32) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = reinterpret_cast<const float4*>(src)[j];
+            for (int j = 0; j < 8; ++j) dst[j] = ld_global_v4_hint(src + 4 * j, pol);
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -204,7 +208,7 @@ __device__ __forceinline__ void epi_f32_direct(float* out_row, bool row_ok, int 
         const int rem = rem0 - c * 32;
         if (row_ok && rem >= 32) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) reinterpret_cast<float4*>(dst)[j] = val[j];
+            for (int j = 0; j < 8; ++j) st_global_v4_hint(dst + 4 * j, val[j], pol);
         } else if (row_ok) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
