@@ -4,8 +4,7 @@
 // tiles of 256 x 256 (128 x 256) in a grouped raster order.
 //   warp 0      : TMA producer -- one thread loads the A and B slices of each
 //                 64-deep K-block into a shared-memory ring (6 stages with a
-//                 CTA pair, 7 for fp32 outputs, which need no staging boxes;
-//                 4 stages for a single CTA).  B may come in two segments
+//                 CTA pair, 4 for a single CTA).  B may come in two segments
 //                 (two weight tiles in different ring slots).
 //   warp 1      : MMA issuer -- one thread issues tcgen05.mma (M=256 across
 //                 the pair or 128, N=256, K=16, bf16 x bf16 -> fp32) into one

@@ -35,8 +35,9 @@ struct Geo {
     static constexpr uint32_t kStageB = uint32_t(kBRows) * kBlockK * 2;
     static constexpr uint32_t kStageBytes = kStageA + kStageB;
     static constexpr uint32_t kEpiBytes = 4u * EPI_BOXES * kEpiBuf;
-    // fp32 outputs need no staging boxes: their shared memory buys a 7th stage
-    static constexpr int kStages = PAIR ? (EPI_BOXES == 0 ? 7 : 6) : 4;
+    // 6 stages in pair mode: a 7th (room for it exists with fp32 outputs,
+    // which need no staging boxes) measured 0.6 % slower on the dX GEMM
+    static constexpr int kStages = PAIR ? 6 : 4;
     static constexpr size_t kSmem = size_t(kStages) * kStageBytes + kEpiBytes + kBarBytes + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
 };
