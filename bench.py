@@ -570,9 +570,12 @@ def run_ours(args, cfg, dist: Dist):
     import __graft_entry__ as g
     from offload_streamed_gb300 import tiled_linear as tl
 
-    if dist.rank == 0 or dist.world > 1:
-        g.build()
     torch.cuda.set_device(dist.local_rank)
+    if dist.rank == 0:  # one rank builds; the others find the library fresh after the barrier
+        g.build()
+    dist.barrier()
+    if dist.rank != 0:
+        g.build()
     peaks = load_peaks()
     T, K, M, N, d = cfg["T"], cfg["K"], cfg["M"], cfg["N"], cfg["d"]
     Mi = M // N
