@@ -304,7 +304,7 @@ def time_resident_compute(tl, cfg, x, dy, w_dev, steps: int):
     y = torch.empty(T, M, dtype=torch.bfloat16, device="cuda")
     dx = torch.empty(T, K, dtype=torch.float32, device="cuda")
     stage = torch.empty(2, K, Mi, dtype=torch.bfloat16, device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    err = torch.zeros(2, dtype=torch.int32, device="cuda")
     s = torch.cuda.current_stream()
     st = s.cuda_stream
 
@@ -333,7 +333,7 @@ def time_resident_compute(tl, cfg, x, dy, w_dev, steps: int):
         step()
     e1.record(s)
     torch.cuda.synchronize()
-    assert int(err.item()) == 0
+    assert int(err[0].item()) == 0
     return e0.elapsed_time(e1) / steps
 
 
@@ -467,15 +467,15 @@ def profile_gemms(cfg, reps: int) -> None:
     y = torch.empty(T, Mi, dtype=torch.bfloat16, device="cuda")
     dw = torch.empty(K, Mi, dtype=torch.bfloat16, device="cuda")
     dx = torch.zeros(T, K, dtype=torch.float32, device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    err = torch.zeros(2, dtype=torch.int32, device="cuda")
     st = torch.cuda.current_stream().cuda_stream
     for _ in range(reps):
         tl.tiled_linear_gemm_forward(T, K, Mi, x.data_ptr(), K, w1.data_ptr(), Mi, y.data_ptr(), Mi, err.data_ptr(), st)
         tl.tiled_linear_gemm_dw(T, K, Mi, x.data_ptr(), K, dy.data_ptr(), nx, dw.data_ptr(), Mi, err.data_ptr(), st)
         tl.tiled_linear_gemm_dx(T, K, nx, dy.data_ptr(), nx, w.data_ptr(), nx, dx.data_ptr(), K, 1, err.data_ptr(), st)
     torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise SystemExit(f"profile_gemms: kernel timeout word {int(err.item())}")
+    if int(err[0].item()) != 0:
+        raise SystemExit(f"profile_gemms: kernel timeout word {int(err[0].item())}")
     log(f"[bench] profile-gemms: {reps} x (fwd, dW, dX over {nx} columns) at T={T} K={K} Mi={Mi}")
 
 

@@ -310,11 +310,16 @@ tl_status tiled_linear_chain_backward(tl_handle *h, int64_t T, const void *x_dev
 
 /* --- resident GEMMs: the three kernels on device-resident operands --------
  * The same kernels the engine launches per tile, for callers that already
- * hold a tile on the device.  fp32 accumulation in tensor memory; err_dev is
- * a device int32 the kernel sets non-zero if a bounded wait gives up (it is
- * only ever OR-ed into, never cleared).  Requirements: every leading
- * dimension and column offset a multiple of 8 elements, pointers 16-byte
- * aligned, all sizes >= 1.  Errors: TL_ERR_INVALID, TL_ERR_CUDA. */
+ * hold a tile on the device.  fp32 accumulation in tensor memory.  err_dev
+ * points to two device int32 words, zeroed by the caller before first use:
+ * err_dev[0] is set non-zero if a bounded wait gives up (it is only ever
+ * OR-ed into, never cleared); err_dev[1] is the counter the CTAs draw output
+ * tiles from (dynamic schedule), which every launch that completes without a
+ * timeout leaves at zero -- after a timeout, zero both words again.  Calls
+ * that may run at the same time (different streams) need separate err
+ * buffers.  Requirements: every leading dimension and column offset a
+ * multiple of 8 elements, pointers 16-byte aligned, all sizes >= 1.
+ * Errors: TL_ERR_INVALID, TL_ERR_CUDA. */
 
 /* y[T, n] (bf16, ld ldy) = x[T, K] (bf16, ld ldx) . w[K, n] (bf16, ld ldw). */
 tl_status tiled_linear_gemm_forward(int64_t T, int64_t K, int64_t n,
@@ -340,10 +345,11 @@ tl_status tiled_linear_gemm_dx(int64_t T, int64_t K, int64_t n,
  * on a 128 x 256 x 64 problem with every operand load withheld and every
  * bounded wait limited to timeout_ns (0 < timeout_ns <= 10 s): the MMA
  * thread's wait for its first shared-memory stage runs out, it sets bit 2 in
- * the int32 at scratch_dev (cleared first), every role stops, the kernel
- * frees its tensor memory and exits -- nothing faults or hangs and the
- * context stays usable.  scratch_dev: device memory, 256-byte aligned, at
- * least 65792 bytes (only the first int32 is written).  Stream-ordered.
+ * the int32 at scratch_dev (cleared first, with the tile counter after it),
+ * every role stops, the kernel frees its tensor memory and exits -- nothing
+ * faults or hangs and the context stays usable.  scratch_dev: device memory,
+ * 256-byte aligned, at least 65792 bytes (only the first two int32 are
+ * written).  Stream-ordered.
  * Errors: TL_ERR_INVALID, TL_ERR_CUDA. */
 tl_status tiled_linear_selftest_timeout(void *scratch_dev, size_t scratch_bytes, int64_t timeout_ns,
                                         void *stream);

@@ -44,6 +44,7 @@ namespace {
 // Workspace header: the kernels' error word, then the persistent pass's
 // sequence flags and per-position counters (zeroed per call).
 constexpr size_t kHeaderBytes = 65536;
+constexpr size_t kTileCounterOffset = 64;
 constexpr size_t kFlagsOffset = 256;
 constexpr size_t kDoneOffset = 4096;
 constexpr size_t kDwDoneOffset = kDoneOffset + 4 * size_t(tl::kMaxPassTiles);
@@ -205,6 +206,7 @@ struct tl_handle {
     uint32_t* done = nullptr;
     uint32_t* dwdone = nullptr;
     uint32_t* dxdone = nullptr;
+    uint32_t* tile_counter = nullptr;   // dynamic tile schedule of the per-tile GEMMs (header word)
     cudaEvent_t ev_d2h_tail = nullptr;  // last dW write-back of the last backward call
     cudaEvent_t ev_call_done = nullptr; // end of the last call (calls share the pass counters)
     Phase fwd, bwd;
@@ -511,7 +513,9 @@ tl_status launch_pass(tl_handle* h, const tl::PassDesc& d, cudaStream_t cs) {
     return TL_OK;
 }
 
-tl_status launch(tl_handle* h, const tl::GemmDesc& g, cudaStream_t st) {
+tl_status launch(tl_handle* h, const tl::GemmDesc& g0, cudaStream_t st) {
+    tl::GemmDesc g = g0;
+    g.tile_counter = h->tile_counter;  // one word: launches on the compute stream are ordered
     std::string why;
     cudaError_t e = tl::gemm_launch(g, h->num_sms, st, &why);
     if (e != cudaSuccess) return fail(h, TL_ERR_CUDA, "GEMM launch: " + why);
@@ -606,6 +610,7 @@ tl_status create_ops(tl_handle** out, std::vector<Op> ops, int32_t d, void* ws, 
     h->done = reinterpret_cast<uint32_t*>(h->ws + kDoneOffset);
     h->dwdone = reinterpret_cast<uint32_t*>(h->ws + kDwDoneOffset);
     h->dxdone = reinterpret_cast<uint32_t*>(h->ws + kDxDoneOffset);
+    h->tile_counter = reinterpret_cast<uint32_t*>(h->ws + kTileCounterOffset);
     uint8_t* p = h->ws + kHeaderBytes;
     for (int s = 0; s < h->slot_cap; ++s, p += tb) h->slot.push_back(p);
     reset_ring(h);
@@ -1467,7 +1472,11 @@ tl_status tiled_linear_reset_stats(tl_handle* h) {
 }
 
 // ---- resident GEMMs --------------------------------------------------------
-static tl_status raw_launch(const tl::GemmDesc& g, void* stream) {
+static tl_status raw_launch(const tl::GemmDesc& g0, void* stream) {
+    tl::GemmDesc g = g0;
+    // the caller's err buffer holds the error word and, next to it, the
+    // tile counter of the dynamic schedule
+    g.tile_counter = g.err ? reinterpret_cast<uint32_t*>(g.err + 1) : nullptr;
     std::string bad = tl::gemm_check(g);
     if (!bad.empty()) return TL_ERR_INVALID;
     int dev = 0, sms = 0;
@@ -1548,7 +1557,7 @@ tl_status tiled_linear_selftest_timeout(void* scratch_dev, size_t scratch_bytes,
         return TL_ERR_INVALID;
     auto* base = static_cast<uint8_t*>(scratch_dev);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(base, 0, sizeof(int32_t), cs) != cudaSuccess) return TL_ERR_CUDA;
+    if (cudaMemsetAsync(base, 0, 2 * sizeof(int32_t), cs) != cudaSuccess) return TL_ERR_CUDA;
     // A 128 x 256 x 64 forward GEMM whose operands are never read: the
     // producer withholds every load, so the MMA thread's first bounded wait
     // runs out.

@@ -50,6 +50,7 @@ struct KParams {
     int32_t accumulate;
     int32_t withhold_loads;
     int32_t* err;
+    uint32_t* tile_counter;  // dynamic schedule (nullptr: static round robin)
     uint64_t timeout_ns;
 };
 
@@ -64,8 +65,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
+    constexpr int Q = 4;  // depth of the tile queue (dynamic schedule)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * G::kStageBytes + G::kEpiBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    int32_t* tile_q = reinterpret_cast<int32_t*>(bars + 2 * S + 5 + 2 * Q);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_q + Q);
+    static_assert((2 * S + 5 + 2 * Q) * 8 + 4 * Q + 4 <= int(kBarBytes), "barrier area");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -82,6 +86,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * S + a); };
     auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+    // Dynamic schedule: the first CTA's producer draws tiles from a device
+    // counter and publishes them in a small queue (tile_q, in both CTAs of a
+    // pair); queue_full[q] (every CTA) says slot q holds a tile id,
+    // queue_empty[q] (first CTA) collects the readers' releases.  An id < 0
+    // ends the sequence.  Without a counter every role walks the static
+    // round robin first_tile, first_tile + tile_step, ...
+    auto qfull_bar = [&](uint32_t q) { return bar0 + 8u * (2 * S + 5 + q); };
+    auto qempty_bar = [&](uint32_t q) { return bar0 + 8u * (2 * S + 5 + Q + q); };
+    const bool dynamic = p.tile_counter != nullptr;
+    constexpr uint32_t kQueueReaders = PAIR ? 10u : 5u;  // MMA, peer producer, epilogue warps
+    auto static_tile = [&](int it) {
+        const int t = first_tile + it * tile_step;
+        return t < p.num_tiles ? t : -1;
+    };
+    // first CTA's producer: draw and publish the tile of iteration `it`
+    auto publish_tile = [&](int it) -> int {
+        const uint32_t q = uint32_t(it) % Q, ph = (uint32_t(it) / Q) & 1u;
+        if (!wait_bounded_cluster(qempty_bar(q), ph ^ 1u, wc, kErrTileQueueWait)) return -1;
+        const uint32_t ticket = atomicAdd(p.tile_counter, 1u);
+        const int t = ticket < uint32_t(p.num_tiles) ? int(ticket) : -1;
+        // every cluster draws once past the end; the last such draw resets
+        // the counter for the next launch
+        if (ticket == uint32_t(p.num_tiles) + uint32_t(tile_step) - 1u) atomicExch(p.tile_counter, 0u);
+        tile_q[q] = t;
+        mbar_arrive_cluster(map_to_rank(qfull_bar(q), 0));
+        if constexpr (PAIR) {
+            st_shared_cluster_u32(map_to_rank(smem_addr(tile_q + q), 1), uint32_t(t));
+            mbar_arrive_cluster(map_to_rank(qfull_bar(q), 1));
+        }
+        return t;
+    };
+    // every other role: read the tile of iteration `it` and release the slot
+    auto take_tile = [&](int it) -> int {
+        const uint32_t q = uint32_t(it) % Q, ph = (uint32_t(it) / Q) & 1u;
+        if (!wait_bounded_cluster(qfull_bar(q), ph, wc, kErrTileQueueWait)) return -1;
+        const int t = *reinterpret_cast<volatile int32_t*>(tile_q + q);
+        mbar_arrive_cluster(map_to_rank(qempty_bar(q), 0));
+        return t;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -93,6 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty_bar(a), PAIR ? 8 : 4);  // one arrival per epilogue warp of the tile
         }
         mbar_init(drain_bar, 1);
+        for (int q = 0; q < Q; ++q) {
+            mbar_init(qfull_bar(q), 1);
+            mbar_init(qempty_bar(q), kQueueReaders);
+        }
         mbar_init_fence();
     }
     if (warp == 2) {
@@ -115,8 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_a = p.raster == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
             const uint64_t pol_b = p.raster == 0 ? l2_policy_evict_first() : l2_policy_evict_last();
             uint32_t fills = 0;
-            bool ok = p.withhold_loads == 0;  // the failure-path self-test withholds every load
-            for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step) {
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int tile = !dynamic ? static_tile(it) : leader ? publish_tile(it) : take_tile(it);
+                if (tile < 0) break;
+                if (p.withhold_loads != 0) break;  // the failure-path self-test withholds every load
                 int mb, nb;
                 tile_coords(tile, p.num_m, p.num_n, p.raster, p.group, mb, nb);
                 const int m0 = mb * G::kTileM + int(rank) * kBlockM;
@@ -170,8 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(G::kTileM, kBlockN, A_MN, B_MN);
             uint32_t fills = 0;
             bool ok = true;
-            int it = 0;
-            for (int tile = first_tile; ok && tile < p.num_tiles; tile += tile_step, ++it) {
+            for (int it = 0; ok; ++it) {
+                const int tile = dynamic ? take_tile(it) : static_tile(it);
+                if (tile < 0) break;
                 const uint32_t acc = it & 1;
                 const uint32_t acc_ph = (it >> 1) & 1;
                 if (!wait_bounded(tempty_bar(acc), acc_ph ^ 1u, wc, kErrMmaWaitTmem)) break;
@@ -217,8 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t epi0 = smem0 + S * G::kStageBytes + uint32_t(q) * 2u * kEpiBuf;
         if (!OUT_F32 && lane == 0) tma_prefetch_map(&map_d);
         uint32_t buf = 0;
-        int it = 0;
-        for (int tile = first_tile; tile < p.num_tiles; tile += tile_step, ++it) {
+        for (int it = 0;; ++it) {
+            int tile;
+            if (dynamic) {
+                int t = 0;
+                if (lane == 0) t = take_tile(it);
+                tile = __shfl_sync(0xffffffffu, t, 0);
+            } else {
+                tile = static_tile(it);
+            }
+            if (tile < 0) break;
             const uint32_t acc = it & 1;
             const uint32_t acc_ph = (it >> 1) & 1;
             int mb, nb;
@@ -385,6 +444,7 @@ std::string gemm_check(const GemmDesc& g) {
     if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.d))
         return "operand pointers must be 16-byte aligned";
     if (reinterpret_cast<uintptr_t>(g.err) & 3u) return "err pointer must be 4-byte aligned";
+    if (reinterpret_cast<uintptr_t>(g.tile_counter) & 3u) return "tile counter must be 4-byte aligned";
     if (g.lda % 8 || g.ldb % 8 || g.ldd % 8)
         return "leading dimensions must be multiples of 8 elements";
     if ((g.a_mn_major ? g.m_dim : g.k_dim) > g.lda) return "A leading dimension too small";
@@ -447,6 +507,7 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     kp.accumulate = g.accumulate ? 1 : 0;
     kp.withhold_loads = g.withhold_loads ? 1 : 0;
     kp.err = g.err;
+    kp.tile_counter = g.tile_counter;
     kp.timeout_ns = g.timeout_ns;
     const int slots = pair ? num_sms / 2 : num_sms;
     const int units = kp.num_tiles < slots ? kp.num_tiles : slots;

@@ -38,6 +38,10 @@ struct GemmDesc {
     OutKind out = OutKind::BF16;
     bool accumulate = false;  // F32 only: D += A.B
     int32_t* err = nullptr;   // device word for bounded-wait timeouts
+    // Device word the CTAs draw output tiles from (dynamic schedule); zero
+    // before the launch, and left zero by a launch that completes without a
+    // timeout.  nullptr: a static round-robin schedule.
+    uint32_t* tile_counter = nullptr;
     uint64_t timeout_ns = 2000000000ull;  // limit of every bounded wait
     bool withhold_loads = false;  // failure-path self-test: the producer issues no loads
 };
@@ -115,6 +119,7 @@ enum : int32_t {
     kErrEpilogueWait = 8,
     kErrDrainWait = 16,
     kErrFlagWait = 32,  // a persistent pass gave up waiting for a copy-stream flag
+    kErrTileQueueWait = 64,  // a role gave up waiting for the next tile of the dynamic schedule
 };
 
 }  // namespace tl

@@ -73,6 +73,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     return wait_slow(bar, parity, w.err, code, stop_on_error, downstream ? 2 * w.timeout_ns : w.timeout_ns);
 }
 
+// Bounded wait with cluster-scope acquire (the dynamic tile queue).
+__device__ __noinline__ inline bool wait_bounded_cluster(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                         int32_t code) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((n & 255u) == 0) {
+            if (*reinterpret_cast<volatile int32_t*>(w.err) != 0) return false;
+            if (global_timer_ns() - t0 > 2 * w.timeout_ns) {
+                atomicOr(w.err, code);
+                return false;
+            }
+        }
+    }
+}
+
 // Warp-uniform wait: lane 0 waits (bounded); then every lane observes the
 // completed phase itself, which cannot move on before this warp arrives.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, int32_t code,

@@ -100,7 +100,7 @@ extern "C" tl_status tiled_linear_forward_static(int64_t T, int64_t K, int64_t M
 
     // The array keeps the previous call's contents: the timeout word must
     // start at zero for this call.
-    if ((e = cudaMemsetAsync(err, 0, sizeof(int32_t), cs)) != cudaSuccess)
+    if ((e = cudaMemsetAsync(err, 0, 2 * sizeof(int32_t), cs)) != cudaSuccess)
         return reject(TL_ERR_CUDA, "clearing the timeout word failed");
     const auto* w = static_cast<const unsigned char*>(w_host);
     for (int32_t i = 0; i < N; ++i) {
@@ -120,6 +120,7 @@ extern "C" tl_status tiled_linear_forward_static(int64_t T, int64_t K, int64_t M
         g.ldd = M;
         g.out = tl::OutKind::BF16;
         g.err = err;
+        g.tile_counter = reinterpret_cast<uint32_t*>(err + 1);
         std::string why;
         if (tl::gemm_launch(g, sms, cs, &why) != cudaSuccess)
             return reject(TL_ERR_CUDA, "kernel launch failed");

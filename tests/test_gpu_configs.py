@@ -75,11 +75,11 @@ def _run_config(tl, T, K, M, N, depths, seed=0, untiled=True):
         # untiled product: one resident GEMM over the whole logical W [K, M]
         w_dev = w.tensor.view(N, K, Mi).to("cuda").permute(1, 0, 2).reshape(K, M).contiguous()
         y_full = torch.empty(T, M, dtype=torch.bfloat16, device="cuda")
-        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        err = torch.zeros(2, dtype=torch.int32, device="cuda")
         tl.tiled_linear_gemm_forward(T, K, M, x.data_ptr(), K, w_dev.data_ptr(), M, y_full.data_ptr(), M,
                                      err.data_ptr(), torch.cuda.current_stream().cuda_stream)
         torch.cuda.synchronize()
-        assert int(err.item()) == 0
+        assert int(err[0].item()) == 0
         assert torch.equal(y_full.view(torch.int16), first[0].view(torch.int16))
         del w_dev, y_full
     w.close()
