@@ -675,6 +675,19 @@ def run_ours(args, cfg, dist: Dist):
                       "l2": "inputs larger than L2: W streamed from host every pass, X 128 MiB+, dY 512 MiB+"},
            "gpu_launches": launches}
     out["value"] = round(dist.world * flops_step / (ms / 1e3) / 1e12, 2)
+    # where the timed region's time went, from the engine's per-launch and
+    # per-copy events summed over every timed call
+    gemm_ms = st["sum_fwd_gemm_ms"] + st["sum_bwd_dw_gemm_ms"] + st["sum_bwd_dx_gemm_ms"]
+    if persistent:
+        gemm_ms = st["sum_fwd_gemm_ms"] + st["sum_bwd_gemm_ms"]
+    h2d_ms = st["sum_fwd_h2d_ms"] + st["sum_bwd_h2d_ms"]
+    out["timed_region"] = {
+        "gemm_ms_per_step": round(gemm_ms / max(fc, 1), 4),
+        "compute_stream_idle_pct": round(100.0 * max(0.0, 1.0 - gemm_ms / max(fc, 1) / ms_local), 2),
+        "h2d_gbs_per_copy": round((st["fwd_h2d_bytes"] + st["bwd_h2d_bytes"]) * fc / (h2d_ms / 1e3) / 1e9, 1)
+        if h2d_ms > 0 else None,
+        "d2h_gbs_per_copy": round(st["bwd_d2h_bytes"] * bc / (st["sum_bwd_d2h_ms"] / 1e3) / 1e9, 1)
+        if st["sum_bwd_d2h_ms"] > 0 else None}
 
     # --- copy-only and resident-compute references ---------------------------
     exposed = None
