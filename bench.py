@@ -292,15 +292,24 @@ def time_copy_schedule(cfg, w, dw, reps: int = 3):
     return min(ts)
 
 
+def dx_group(d: int, N: int, Mi: int) -> int:
+    """Tiles per dX launch at depth d: the engine's rule (tiled_linear.h,
+    backward), max(2, ceil(8192 / Mi)) bounded by d + 1, N and 4."""
+    d = min(d, N - 1)
+    if d < 1 or N < 2 or Mi % 64:
+        return 1
+    return min(max(2, -(-8192 // Mi)), d + 1, N, 4)
+
+
 def time_resident_compute(tl, cfg, x, dy, w_dev, steps: int):
     """t_compute_resident: the step's GEMM sequence (the same kernels, same
-    order, dX over the same tile pairs) on W already in HBM (row-major
-    [K, M], so a pair of tiles is one column block), through the
+    order, dX over the same tile groups) on W already in HBM (row-major
+    [K, M], so a group of tiles is one column block), through the
     resident-GEMM ABI."""
     import torch
     T, K, M, N, d = cfg["T"], cfg["K"], cfg["M"], cfg["N"], cfg["d"]
     Mi = M // N
-    pairs = d != 0 and N >= 2 and Mi % 64 == 0
+    gsz = dx_group(d, N, Mi)
     y = torch.empty(T, M, dtype=torch.bfloat16, device="cuda")
     dx = torch.empty(T, K, dtype=torch.float32, device="cuda")
     stage = torch.empty(2, K, Mi, dtype=torch.bfloat16, device="cuda")
@@ -312,17 +321,18 @@ def time_resident_compute(tl, cfg, x, dy, w_dev, steps: int):
         for i in range(N):
             tl.tiled_linear_gemm_forward(T, K, Mi, x.data_ptr(), K, w_dev[:, i * Mi:].data_ptr(), M,
                                          y[:, i * Mi:].data_ptr(), M, err.data_ptr(), st)
-        nx = 0
+        nx, pend = 0, 0
         for j in range(N):
             i = N - 1 - j
             tl.tiled_linear_gemm_dw(T, K, Mi, x.data_ptr(), K, dy[:, i * Mi:].data_ptr(), M,
                                     stage[j % 2].data_ptr(), Mi, err.data_ptr(), st)
-            if pairs and j % 2 == 0 and j + 1 < N:
-                continue  # reduced together with the next tile
-            w = 2 * Mi if (pairs and j % 2 == 1) else Mi
+            if pend + 1 < gsz and j + 1 < N:
+                pend += 1
+                continue  # reduced together with the next tiles
+            w = (pend + 1) * Mi
             tl.tiled_linear_gemm_dx(T, K, w, dy[:, i * Mi:].data_ptr(), M, w_dev[:, i * Mi:].data_ptr(), M,
                                     dx.data_ptr(), K, nx > 0, err.data_ptr(), st)
-            nx += 1
+            nx, pend = nx + 1, 0
 
     for _ in range(2):
         step()
@@ -446,7 +456,7 @@ def load_traffic(config: str) -> dict:
 
 
 def profile_gemms(cfg, reps: int) -> None:
-    """The three resident GEMMs of one tile (dX of one tile pair, as a step
+    """The three resident GEMMs of one tile (dX of one tile group, as a step
     runs it) of the workload, `reps` times in the order fwd, dW, dX: a small
     fixed launch sequence for ncu captures of each kernel (inputs above L2,
     under 1 GiB on the device)."""
@@ -459,10 +469,10 @@ def profile_gemms(cfg, reps: int) -> None:
     g.build()
     T, K, M, N = cfg["T"], cfg["K"], cfg["M"], cfg["N"]
     Mi = M // N
-    nx = 2 * Mi if (cfg["d"] != 0 and N >= 2 and Mi % 64 == 0) else Mi
+    nx = dx_group(cfg["d"], N, Mi) * Mi
     x = I.make_x(T, K, 0, device="cuda")
     dy = I.make_dy(T, nx, 0, device="cuda")
-    w = I.make_w_tile(K, nx, 0, 0, device="cuda")   # a tile pair, row-major [K, nx]
+    w = I.make_w_tile(K, nx, 0, 0, device="cuda")   # a tile group, row-major [K, nx]
     w1 = w[:, :Mi].contiguous()                      # one tile, as a ring slot holds it
     y = torch.empty(T, Mi, dtype=torch.bfloat16, device="cuda")
     dw = torch.empty(K, Mi, dtype=torch.bfloat16, device="cuda")
@@ -620,7 +630,7 @@ def run_ours(args, cfg, dist: Dist):
     st = op.stats()
     persistent = bool(st.get("persistent", 0))
     launches = args.steps * (st["fwd_launches"] + st["bwd_launches"])
-    n_dx = max(st["bwd_launches"] - N, 1)  # dX launches per backward (tile pairs)
+    n_dx = max(st["bwd_launches"] - N, 1)  # dX launches per backward (tile groups)
 
     # --- per-kernel averages over the timed region ---------------------------
     fc, bc = max(st["fwd_calls"], 1), max(st["bwd_calls"], 1)
@@ -631,11 +641,11 @@ def run_ours(args, cfg, dist: Dist):
         flops_launch = 2.0 * T * K * Mi
         kern = {"fwd_gemm (Y_i = X.W_i)": (st["sum_fwd_gemm_ms"] / (fc * N), flops_launch),
                 "dw_gemm (dW_i = X^T.dY_i)": (st["sum_bwd_dw_gemm_ms"] / (bc * N), flops_launch),
-                "dx_gemm (dX += dY_i.W_i^T over a tile pair)": (st["sum_bwd_dx_gemm_ms"] / (bc * n_dx),
+                "dx_gemm (dX += dY_i.W_i^T over a tile group)": (st["sum_bwd_dx_gemm_ms"] / (bc * n_dx),
                                                                  2.0 * T * K * M / n_dx)}
     count = {k: (1 if persistent else N) for k in kern}
     if not persistent:
-        count["dx_gemm (dX += dY_i.W_i^T over a tile pair)"] = n_dx
+        count["dx_gemm (dX += dY_i.W_i^T over a tile group)"] = n_dx
     dom = max(kern, key=lambda k: kern[k][0] * count[k])
     peak = peaks["bf16_tflops_sustained"]
     dom_ms, dom_flops = kern[dom]
@@ -653,14 +663,15 @@ def run_ours(args, cfg, dist: Dist):
         # algorithmic HBM bytes per launch (operands once, outputs once, the
         # dX read-modify-write) and the ncu-measured DRAM bytes, if current
         kind = dom.split(" ")[0]
-        nx = 2 * Mi if n_dx * 2 == N else Mi
+        g = dx_group(d, N, Mi)
+        nx = M // n_dx  # reduction width of the average dX launch
         algo = {"fwd_gemm": 2 * T * K + 2 * K * Mi + 2 * T * Mi,
                 "dw_gemm": 2 * T * K + 2 * T * Mi + 2 * K * Mi,
                 "dx_gemm": 2 * T * nx + 2 * K * nx + 8 * T * K}[kind]
         roofline["algorithmic_bytes_per_launch"] = algo
         traffic = load_traffic(args.config)
-        key = {"fwd_gemm": "fwd_gemm", "dw_gemm": "dw_gemm", "dx_gemm": "dx_gemm_pair"}[kind]
-        if nx == 2 * Mi or kind != "dx_gemm":
+        key = {"fwd_gemm": "fwd_gemm", "dw_gemm": "dw_gemm", "dx_gemm": "dx_gemm_group"}[kind]
+        if kind != "dx_gemm" or N % g == 0:  # the profile captured a full group
             roofline["traffic"] = traffic.get(key + "_bytes_per_launch")
         roofline["traffic_source"] = "profiles/dram_traffic_gpt_tile.txt (ncu dram__bytes_read.sum + " \
                                      "dram__bytes_write.sum; null when the kernel sources changed since)"

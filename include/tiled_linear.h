@@ -144,11 +144,13 @@ tl_status tiled_linear_forward(tl_handle *h, int64_t T, const void *x_dev, void 
 /* Backward, tiles in descending order i = N-1 .. 0:
  *   dW_i = X^T . dY_i  (fp32 accumulation, bf16 RNE) -> dw_host tile i
  *   dx_dev[T, K] (fp32, ld K) = sum_i dY_i . W_i^T   (overwritten).  Fixed
- *   summation order: when d >= 1, N >= 2 and Mi % 64 == 0, tiles go in pairs
- *   (N-1, N-2), (N-3, N-4), ...; each pair is reduced in one fp32 accumulator
- *   over its columns in ascending order, the first pair stores, later pairs
- *   (and a lone tile 0 when N is odd) add.  Otherwise the first tile stores
- *   and later tiles add one at a time.  Both launch modes use this order.
+ *   summation order: when d >= 1, N >= 2 and Mi % 64 == 0, tiles go in
+ *   groups of g = min(max(2, ceil(8192 / Mi)), d+1, N, 4) consecutive tiles,
+ *   (N-1 .. N-g), (N-g-1 .. N-2g), ..., the last group holding what is
+ *   left; each group is reduced
+ *   in one fp32 accumulator over its columns in ascending order, the first
+ *   group stores, later groups add.  Otherwise the first tile stores and
+ *   later tiles add one at a time.  Both launch modes use this order.
  * dy_dev is [T, M] bf16 (ld M).  T = 0 writes dW = 0.  dW on the host is
  * complete once `stream` has completed.  Errors as tiled_linear_forward. */
 tl_status tiled_linear_backward(tl_handle *h, int64_t T, const void *x_dev,

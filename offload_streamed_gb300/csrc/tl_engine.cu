@@ -460,10 +460,21 @@ tl_status finish_auto_depth(tl_handle* h) {
 CUstream cu(cudaStream_t s) { return reinterpret_cast<CUstream>(s); }
 CUdeviceptr cuptr(const void* p) { return reinterpret_cast<CUdeviceptr>(p); }
 
-// dX is accumulated over pairs of tiles when the ring holds two tiles (d >= 1)
-// and the tile width splits into whole 64-deep K-blocks.  Both launch modes
-// use the same pairs, so their dX agree bit for bit.
-bool dx_pairs(const tl_handle* h, const Shape& s) { return h->d >= 1 && s.N >= 2 && s.Mi % tl::kBlockK == 0; }
+// dX is accumulated over groups of consecutive tiles, one launch per group,
+// whenever the ring holds several tiles (d >= 1) and the tile width splits
+// into whole 64-deep K-blocks.  A group reduces at least 8192 deep where the
+// ring allows: g = max(2, ceil(8192 / Mi)), at most d + 1, N and 4 (the
+// GEMM's B segments); the last group of an operator may be smaller.  Pairs
+// for wide tiles: a larger group holds more of the ring and delays the next
+// fetches (groups of three measured 1 % slower on the GPT-scale layer), while
+// narrow tiles need the depth (groups of three: +7 % on the FFN chain, whose
+// down-projection has 1024-wide tiles).  Both launch modes use the same
+// groups, so their dX agree bit for bit.
+int dx_group(const tl_handle* h, const Shape& s) {
+    if (h->d < 1 || s.N < 2 || s.Mi % tl::kBlockK) return 1;
+    const int want = std::max<int>(2, int((8192 + s.Mi - 1) / s.Mi));
+    return std::min({want, h->d + 1, s.N, int(tl::GemmDesc::kMaxSeg)});
+}
 
 tl::PassDesc pass_desc(const tl_handle* h, bool backward, int64_t T, uint64_t fetch_base, uint64_t stage_base) {
     tl::PassDesc d;
@@ -478,7 +489,7 @@ tl::PassDesc pass_desc(const tl_handle* h, bool backward, int64_t T, uint64_t fe
     for (int g = 0; g < d.nstage && g < tl::kMaxPassStages; ++g) d.stages[g] = h->stage[g];
     d.fetch_base = uint32_t(fetch_base);
     d.stage_base = uint32_t(stage_base);
-    d.dx_group = dx_pairs(h, h->s) ? 2 : 1;
+    d.dx_group = dx_group(h, h->s);
     d.flags = h->flags;
     d.done = h->done;
     d.dwdone = h->dwdone;
@@ -835,7 +846,7 @@ tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys,
 
 // Backward, operators in reverse and each one's tiles in descending order:
 //   dW_{l,i} = X_l^T . dY_l[:, tile i] -> staging slot -> host (d2h stream)
-//   dX_l (+)= dY_l[:, tile i] . W_{l,i}^T in fp32 (tile pairs, see dx_pairs)
+//   dX_l (+)= dY_l[:, tile i] . W_{l,i}^T in fp32 (tile groups, see dx_group)
 // dY_{L-1} = dy; for l < L-1, dY_l = bf16(dX_{l+1}) (cast on the caller's
 // stream into scr_dy), dX_l for l >= 1 accumulates in scr_dx, dX_0 in dx.
 tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* const* ys, const void* dy,
@@ -896,11 +907,10 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
         const void* dyl = l == L - 1 ? dy : scr_dy;
         float* dxl = l == 0 ? dx : scr_dx;
         const size_t tb = tile_bytes(s.K, s.Mi);
-        // dX is accumulated over pairs of tiles (i+1, i) -- one launch
-        // reducing over both, in ascending column order -- whenever the ring
-        // holds two tiles; a lone last tile (N odd) and d = 0 go one at a time.
-        const bool pairs = dx_pairs(h, s);
-        int pend_sl = -1;  // ring slot of the pair's first (higher) tile
+        // dX is accumulated over groups of tiles (i+g-1, ..., i) -- one
+        // launch reducing over all of them, in ascending column order.
+        const int gsz = dx_group(h, s);
+        std::vector<int> pend;  // ring slots of the open group's tiles, highest tile first
         int dx_launches = 0;
         for (int j = 0; j < s.N; ++j, ++jg) {
             const int i = s.N - 1 - j;
@@ -963,30 +973,33 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             TL_TRY(h, cudaEventRecord(h->ev_drained[gs], h->d2h));
             d2h_bytes += int64_t(tb);
 
-            if (pairs && pend_sl < 0 && j + 1 < s.N) {
-                // first tile of a pair: its dX is reduced with the next tile's
-                pend_sl = sl;
+            if (int(pend.size()) + 1 < gsz && j + 1 < s.N) {
+                // not the group's last (lowest) tile: its dX waits for the group
+                pend.push_back(sl);
                 TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
                 TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
                 continue;
             }
-            // dX (+)= dY_i W_i^T (+ dY_{i+1} W_{i+1}^T), fp32; the first launch stores
-            TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
-            if (pend_sl >= 0) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[pend_sl], 0));
+            // dX (+)= sum over the group's tiles i, i+1, .. of dY_i W_i^T, fp32;
+            // the first launch stores
+            std::vector<int> grp(pend.rbegin(), pend.rend());  // ascending tile order from i+1
+            grp.insert(grp.begin(), sl);                        // tile i first
+            for (int gsl : grp) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[gsl], 0));
             TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
             tl::GemmDesc gx;
             gx.m_dim = T;
             gx.n_dim = s.K;
-            gx.k_dim = pend_sl >= 0 ? 2 * s.Mi : s.Mi;
+            gx.k_dim = int64_t(grp.size()) * s.Mi;
             gx.a = static_cast<const uint8_t*>(dyl) + size_t(i) * size_t(s.Mi) * 2;
             gx.lda = s.M;
             gx.a_mn_major = false;
             gx.b = h->slot[sl];
             gx.ldb = s.Mi;
             gx.b_mn_major = false;
-            if (pend_sl >= 0) {  // reduction rows Mi .. 2Mi-1 are tile i+1's
-                gx.b2 = h->slot[pend_sl];
-                gx.k_split = s.Mi;
+            if (grp.size() > 1) {  // reduction rows [j Mi, (j+1) Mi) are tile i+j's
+                gx.nseg = int32_t(grp.size());
+                gx.k_seg = s.Mi;
+                for (size_t jj = 0; jj < grp.size(); ++jj) gx.bseg[jj] = h->slot[size_t(grp[jj])];
             }
             gx.d = dxl;
             gx.ldd = s.K;
@@ -997,13 +1010,13 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             ++dx_launches;
             ++launches;
             TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
-            TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
-            if (pend_sl >= 0) {
-                TL_TRY(h, cudaEventRecord(h->ev_free[pend_sl], cs));
-                h->slot_q.push_back(pend_sl);
+            for (int psl : pend) {
+                TL_TRY(h, cudaEventRecord(h->ev_free[psl], cs));
+                h->slot_q.push_back(psl);
             }
+            TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
             h->slot_q.push_back(sl);
-            pend_sl = -1;
+            pend.clear();
         }
         if (l > 0) {  // dY of the operator before: bf16 RNE of this dX
             std::string why;

@@ -40,11 +40,16 @@ namespace {
 
 using namespace kc;
 
+// Tensor maps of B segments 1.. (segment 0 is map_b).
+struct BSegMaps {
+    CUtensorMap m[GemmDesc::kMaxSeg - 1];
+};
+
 struct KParams {
     int32_t m_dim, n_dim, k_dim;
     int32_t num_m, num_n, num_k, num_tiles;
     int32_t raster, group;  // tile order (see kc::tile_coords)
-    int32_t k_split;        // reduction index where B switches to map_b2 (INT32_MAX: never)
+    int32_t k_seg;          // reduction rows per B segment (INT32_MAX: one segment)
     void* d;
     int64_t ldd;
     int32_t accumulate;
@@ -57,7 +62,7 @@ struct KParams {
 template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const __grid_constant__ CUtensorMap map_d, const __grid_constant__ CUtensorMap map_b2,
+                const __grid_constant__ CUtensorMap map_d, const __grid_constant__ BSegMaps segs,
                 const KParams p) {
     using G = Geo<PAIR, OUT_F32 ? 0 : 2>;
     const WaitCtx wc{p.err, p.timeout_ns};
@@ -156,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- TMA producer (each CTA loads its own halves) ----------------
             tma_prefetch_map(&map_a);
             tma_prefetch_map(&map_b);
-            if (p.k_split < p.k_dim) tma_prefetch_map(&map_b2);
+            for (int j = 1; j < GemmDesc::kMaxSeg && j * p.k_seg < p.k_dim; ++j) tma_prefetch_map(&segs.m[j - 1]);
             // the tile order keeps a group of A blocks (raster 0) or of B
             // blocks (raster 1) in L2; the other operand streams through
             const uint64_t pol_a = p.raster == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
@@ -197,10 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < G::kBRows / 64; ++c)
                             load(sb + c * kMnChunk, &map_b, n0 + 64 * c, k0, pol_b);
-                    } else if (k0 < p.k_split) {
+                    } else if (k0 < p.k_seg) {
                         load(sb, &map_b, k0, n0, pol_b);
-                    } else {  // second B segment
-                        load(sb, &map_b2, k0 - p.k_split, n0, pol_b);
+                    } else {  // a further B segment
+                        const int seg = k0 / p.k_seg;
+                        load(sb, &segs.m[seg - 1], k0 - seg * p.k_seg, n0, pol_b);
                     }
                 }
             }
@@ -363,7 +369,7 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 }
 
 template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
-cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& mb2,
+cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const BSegMaps& segs,
                        const KParams& kp, int grid, cudaStream_t stream) {
     auto kern = gemm_kernel<A_MN, B_MN, OUT_F32, PAIR>;
     constexpr size_t smem = Geo<PAIR, OUT_F32 ? 0 : 2>::kSmem;
@@ -381,16 +387,16 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ma, mb, md, mb2, kp);
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, md, segs, kp);
 }
 
 template <bool PAIR>
 cudaError_t dispatch(const GemmDesc& g, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
-                     const CUtensorMap& mb2, const KParams& kp, int grid, cudaStream_t stream) {
+                     const BSegMaps& segs, const KParams& kp, int grid, cudaStream_t stream) {
     if (!g.a_mn_major && g.b_mn_major)
-        return launch_one<false, true, false, PAIR>(ma, mb, md, mb2, kp, grid, stream);
-    if (g.a_mn_major && g.b_mn_major) return launch_one<true, true, false, PAIR>(ma, mb, md, mb2, kp, grid, stream);
-    return launch_one<false, false, true, PAIR>(ma, mb, md, mb2, kp, grid, stream);
+        return launch_one<false, true, false, PAIR>(ma, mb, md, segs, kp, grid, stream);
+    if (g.a_mn_major && g.b_mn_major) return launch_one<true, true, false, PAIR>(ma, mb, md, segs, kp, grid, stream);
+    return launch_one<false, false, true, PAIR>(ma, mb, md, segs, kp, grid, stream);
 }
 
 
@@ -448,7 +454,7 @@ std::string gemm_check(const GemmDesc& g) {
     if (g.lda % 8 || g.ldb % 8 || g.ldd % 8)
         return "leading dimensions must be multiples of 8 elements";
     if ((g.a_mn_major ? g.m_dim : g.k_dim) > g.lda) return "A leading dimension too small";
-    if (!g.b2 && (g.b_mn_major ? g.n_dim : g.k_dim) > g.ldb) return "B leading dimension too small";
+    if (g.nseg <= 1 && (g.b_mn_major ? g.n_dim : g.k_dim) > g.ldb) return "B leading dimension too small";
     if (g.n_dim > g.ldd) return "D leading dimension too small";
     if (g.lda * 2 >= (int64_t(1) << 40) || g.ldb * 2 >= (int64_t(1) << 40))
         return "leading dimension too large";
@@ -459,12 +465,14 @@ std::string gemm_check(const GemmDesc& g) {
     const bool dx = !g.a_mn_major && !g.b_mn_major && g.out == OutKind::F32;
     if (!(fwd || dw || dx)) return "unsupported operand-major / output combination";
     if (g.accumulate && g.out != OutKind::F32) return "accumulate needs fp32 output";
-    if (g.b2) {
-        if (g.b_mn_major) return "a second B segment needs a K-major B";
-        if (!aligned16(g.b2)) return "operand pointers must be 16-byte aligned";
-        if (g.k_split <= 0 || g.k_split >= g.k_dim || g.k_split % kBlockK)
-            return "k_split must be a multiple of 64 inside (0, k_dim)";
-        if (g.k_dim - g.k_split > g.ldb || g.k_split > g.ldb) return "B leading dimension too small";
+    if (g.nseg < 1 || g.nseg > GemmDesc::kMaxSeg) return "nseg must be in 1..4";
+    if (g.nseg > 1) {
+        if (g.b_mn_major) return "B segments need a K-major B";
+        for (int j = 1; j < g.nseg; ++j)
+            if (!g.bseg[j] || !aligned16(g.bseg[j])) return "B segment pointers must be non-null and 16-byte aligned";
+        if (g.k_seg <= 0 || g.k_seg % kBlockK || g.k_seg * g.nseg != g.k_dim)
+            return "k_seg must be a multiple of 64 with nseg * k_seg == k_dim";
+        if (g.k_seg > g.ldb) return "B leading dimension too small";
     }
     return {};
 }
@@ -482,13 +490,16 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     const bool ok_a = g.a_mn_major ? make_map(&ma, g.a, g.m_dim, g.k_dim, g.lda, 64, why)
                                    : make_map(&ma, g.a, g.k_dim, g.m_dim, g.lda, kBlockM, why);
     if (!ok_a) return cudaErrorInvalidValue;
-    const int64_t k_b = g.b2 ? g.k_split : g.k_dim;  // reduction rows held by b
+    const int64_t k_b = g.nseg > 1 ? g.k_seg : g.k_dim;  // reduction rows held by b
     const bool ok_b = g.b_mn_major ? make_map(&mb, g.b, g.n_dim, k_b, g.ldb, 64, why)
                                    : make_map(&mb, g.b, k_b, g.n_dim, g.ldb, b_rows, why);
     if (!ok_b) return cudaErrorInvalidValue;
-    CUtensorMap mb2 = mb;
-    if (g.b2 && !make_map(&mb2, g.b2, g.k_dim - g.k_split, g.n_dim, g.ldb, b_rows, why))
-        return cudaErrorInvalidValue;
+    BSegMaps segs;
+    for (int j = 1; j < GemmDesc::kMaxSeg; ++j) {
+        segs.m[j - 1] = mb;
+        if (j < g.nseg && !make_map(&segs.m[j - 1], g.bseg[j], g.k_seg, g.n_dim, g.ldb, b_rows, why))
+            return cudaErrorInvalidValue;
+    }
     CUtensorMap md;
     if (!make_map(&md, g.d, g.n_dim, g.m_dim, g.ldd, 32, why, g.out == OutKind::F32)) return cudaErrorInvalidValue;
 
@@ -501,7 +512,7 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     kp.num_k = int32_t((g.k_dim + kBlockK - 1) / kBlockK);
     kp.num_tiles = kp.num_m * kp.num_n;
     choose_tile_order(g.k_dim, tile_m, kp.num_m, kp.num_n, &kp.raster, &kp.group);
-    kp.k_split = g.b2 ? int32_t(g.k_split) : INT32_MAX;
+    kp.k_seg = g.nseg > 1 ? int32_t(g.k_seg) : INT32_MAX;
     kp.d = g.d;
     kp.ldd = g.ldd;
     kp.accumulate = g.accumulate ? 1 : 0;
@@ -513,8 +524,8 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     const int units = kp.num_tiles < slots ? kp.num_tiles : slots;
     const int grid = pair ? 2 * units : units;
 
-    const cudaError_t e = pair ? dispatch<true>(g, ma, mb, md, mb2, kp, grid, stream)
-                               : dispatch<false>(g, ma, mb, md, mb2, kp, grid, stream);
+    const cudaError_t e = pair ? dispatch<true>(g, ma, mb, md, segs, kp, grid, stream)
+                               : dispatch<false>(g, ma, mb, md, segs, kp, grid, stream);
     if (e != cudaSuccess && why) *why = std::string("kernel launch: ") + cudaGetErrorString(e);
     return e;
 }

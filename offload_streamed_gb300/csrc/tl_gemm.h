@@ -27,12 +27,15 @@ struct GemmDesc {
     const void* b = nullptr;
     int64_t ldb = 0;
     bool b_mn_major = false;
-    // Optional second B segment (K-major B only): reduction rows k >= k_split
-    // are read from b2[n * ldb + (k - k_split)] instead of b.  k_split is a
-    // multiple of kBlockK with 0 < k_split < k_dim.  Lets one launch reduce
-    // over two weight tiles that sit in different ring slots.
-    const void* b2 = nullptr;
-    int64_t k_split = 0;
+    // Optional further B segments (K-major B only): with nseg > 1, reduction
+    // rows [j k_seg, (j+1) k_seg) are read from segment j, bseg[j][n * ldb +
+    // (k - j k_seg)], where bseg[0] is b.  k_seg is a multiple of kBlockK and
+    // nseg * k_seg == k_dim.  Lets one launch reduce over several weight
+    // tiles that sit in different ring slots.
+    static constexpr int kMaxSeg = 4;
+    const void* bseg[kMaxSeg] = {};
+    int32_t nseg = 1;
+    int64_t k_seg = 0;
     void* d = nullptr;
     int64_t ldd = 0;
     OutKind out = OutKind::BF16;

@@ -94,8 +94,9 @@ def test_tiny_config_full_parity(tl, tile_major, persistent):
     if persistent:
         assert st["fwd_launches"] == 1 and st["bwd_launches"] == 1
     else:
-        # one dW launch per tile, one dX launch per tile pair
-        assert st["fwd_launches"] == N and st["bwd_launches"] == N + (N + 1) // 2
+        # one dW launch per tile, one dX launch per group of tiles
+        g = dx_group(d, N, M // N)
+        assert st["fwd_launches"] == N and st["bwd_launches"] == N + (N + g - 1) // g
     assert st["fwd_h2d_bytes"] == K * M * 2 and st["bwd_h2d_bytes"] == K * M * 2
     assert st["bwd_d2h_bytes"] == K * M * 2
     assert st["depth"] == d
@@ -119,11 +120,15 @@ def _same(a, b):
                        b.contiguous().view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
 
 
-def dx_group(d, N, Mi):
-    """Tiles per dX accumulation group: both launch modes reduce dX over pairs
-    of tiles whenever the ring holds two (d >= 1) and the tile width is a
-    multiple of 64; otherwise one tile at a time."""
-    return 2 if (d != 0 and N >= 2 and Mi % 64 == 0) else 1
+def dx_group(depth, N, Mi):
+    """Tiles per dX accumulation group for the depth a call ran with (from its
+    stats): both launch modes reduce dX over groups of
+    min(max(2, ceil(8192 / Mi)), depth+1, N, 4) tiles whenever the ring holds
+    several (depth >= 1) and the tile width is a multiple of 64; otherwise one
+    tile at a time."""
+    if not (depth >= 1 and N >= 2 and Mi % 64 == 0):
+        return 1
+    return min(max(2, -(-8192 // Mi)), depth + 1, N, 4)
 
 
 def test_schedule_does_not_change_results(tl):
@@ -132,15 +137,15 @@ def test_schedule_does_not_change_results(tl):
     whose grouping is part of the schedule) is bit-identical among schedules
     with the same dX grouping and matches the oracle for every one."""
     T, K, M, N = 200, 264, 2048, 8
-    base = {1: run_op(tl, T, K, M, N, 0, tile_major=True, seed=7, persistent=False),
-            2: run_op(tl, T, K, M, N, 1, tile_major=True, seed=7, persistent=False)}
-    for r in base.values():
+    base = {g: run_op(tl, T, K, M, N, g - 1, tile_major=True, seed=7, persistent=False) for g in (1, 2, 3, 4)}
+    for g, r in base.items():
+        assert dx_group(r.stats["depth"], N, M // N) == g
         oracle_check(r, T, K, M)
     for d, tm, calls, pers in [(0, True, 1, True), (2, True, 1, True), (3, False, 1, True), (7, True, 2, True),
                                (12, False, 1, True), (-1, True, 3, True), (1, True, 1, False),
                                (0, False, 2, False), (5, True, 1, False), (-1, True, 2, False)]:
         r = run_op(tl, T, K, M, N, d, tile_major=tm, seed=7, calls=calls, persistent=pers)
-        ref = base[dx_group(d, N, M // N)]
+        ref = base[dx_group(r.stats["depth"], N, M // N)]
         assert _same(r.y, ref.y), (d, tm, pers)
         assert _same(r.dw, ref.dw), (d, tm, pers)
         assert _same(r.dx, ref.dx), (d, tm, pers)
@@ -246,7 +251,7 @@ def test_stats_are_consistent(tl, persistent):
               "bwd_d2h_ms"):
         assert st[k] > 0, k
     if not persistent:
-        assert st["bwd_launches"] == N + N // 2
+        assert st["bwd_launches"] == N + (N + 2) // 3  # d = 2: groups of three
         assert st["bwd_dw_gemm_ms"] > 0 and st["bwd_dx_gemm_ms"] > 0
         assert abs(st["bwd_dw_gemm_ms"] + st["bwd_dx_gemm_ms"] - st["bwd_gemm_ms"]) < 1e-3
     assert st["fwd_gemm_ms"] <= st["fwd_total_ms"] + 1e-3
