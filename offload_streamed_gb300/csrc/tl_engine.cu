@@ -148,6 +148,7 @@ struct CallSlot {
     bool harvested = false;
     int32_t nk = 0;        // kernel spans recorded (N per-tile launches, or 1 pass)
     int32_t depth = 0, launches = 0, reused = 0;
+    bool timed = true;     // per-launch and per-copy events recorded (see tiled_linear_set_timing)
     int64_t h2d_bytes = 0, d2h_bytes = 0;
     float total = 0, gemm1 = 0, gemm2 = 0, h2d = 0, d2h = 0;
 };
@@ -159,8 +160,8 @@ struct Phase {
     bool backward = false;
     std::vector<CallSlot> ring;
     uint64_t calls = 0;
-    int last = -1;
-    int64_t sum_calls = 0;
+    int last = -1;        // ring index of the last timed call
+    int64_t sum_calls = 0, sum_timed = 0;
     double sum_total = 0, sum_gemm1 = 0, sum_gemm2 = 0, sum_h2d = 0, sum_d2h = 0;
 };
 
@@ -192,6 +193,7 @@ struct tl_handle {
     std::deque<int> slot_q;
     std::vector<int32_t> slot_tile;
     bool reuse = false;
+    int32_t timing_every = 1;  // record per-launch / per-copy events on every n-th call
     // Host optimizer attached by tiled_linear_optimizer_create: its worker,
     // per-tile events the backward records (W read by the GPU, dW in host
     // memory) and the tile order of the last backward.
@@ -352,6 +354,12 @@ tl_status harvest(tl_handle* h, Phase& p, CallSlot& c, int n) {
     TL_TRY(h, cudaEventSynchronize(c.end));
     c.total = span_ms(c.start, c.end);
     c.gemm1 = c.gemm2 = c.h2d = c.d2h = 0;
+    if (!c.timed) {  // only counted: the sums describe the timed calls
+        c.pending = false;
+        c.harvested = true;
+        p.sum_calls += 1;
+        return TL_OK;
+    }
     for (int i = 0; i < n; ++i) {
         if (i < c.nk) {
             c.gemm1 += span_ms(c.ev[0][i], c.ev[1][i]);
@@ -363,6 +371,7 @@ tl_status harvest(tl_handle* h, Phase& p, CallSlot& c, int n) {
     c.pending = false;
     c.harvested = true;
     p.sum_calls += 1;
+    p.sum_timed += 1;
     p.sum_total += c.total;
     p.sum_gemm1 += c.gemm1;
     p.sum_gemm2 += c.gemm2;
@@ -383,13 +392,15 @@ tl_status harvest_all(tl_handle* h, Phase& p) {
 CallSlot* begin_call(tl_handle* h, Phase& p, tl_status* st) {
     CallSlot& c = p.ring[p.calls % kTimingRing];
     *st = harvest(h, p, c, h->n_total);
-    return *st == TL_OK ? &c : nullptr;
+    if (*st != TL_OK) return nullptr;
+    c.timed = p.calls % uint64_t(h->timing_every) == 0;
+    return &c;
 }
 
 void end_call(Phase& p, CallSlot& c) {
     c.pending = true;
     c.harvested = false;
-    p.last = int(p.calls % kTimingRing);
+    if (c.timed) p.last = int(p.calls % kTimingRing);
     p.calls += 1;
 }
 
@@ -804,15 +815,15 @@ tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys,
             if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
             h->slot_tile[size_t(sl)] = -1;
             TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
-            TL_TRY(h, cudaEventRecord(t.ev[4][g], h->h2d));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[4][g], h->h2d));
             TL_TRY(h, copy_w_tile(o, i, h->slot[sl], h->h2d));
             h->slot_tile[size_t(sl)] = g;
             h2d_bytes += int64_t(tile_bytes(s.K, s.Mi));
-            TL_TRY(h, cudaEventRecord(t.ev[5][g], h->h2d));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[5][g], h->h2d));
             TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
 
             TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[sl], 0));
-            TL_TRY(h, cudaEventRecord(t.ev[0][g], cs));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[0][g], cs));
             tl::GemmDesc gd;
             gd.m_dim = T;
             gd.n_dim = s.Mi;
@@ -828,7 +839,7 @@ tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys,
             gd.out = tl::OutKind::BF16;
             gd.err = h->err_dev;
             if ((st = launch(h, gd, cs)) != TL_OK) return st;
-            TL_TRY(h, cudaEventRecord(t.ev[1][g], cs));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[1][g], cs));
             TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
             h->slot_q.push_back(sl);
         }
@@ -919,17 +930,17 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             int sl;
             if (jg < reused) {  // W_i is still in the ring
                 sl = resident[size_t(g)];
-                TL_TRY(h, cudaEventRecord(t.ev[4][jg], h->h2d));
-                TL_TRY(h, cudaEventRecord(t.ev[5][jg], h->h2d));
+                if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[4][jg], h->h2d));
+                if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[5][jg], h->h2d));
             } else {  // refetch W_i
                 if ((st = opt_wait(h, g, true)) != TL_OK) return st;
                 sl = take_slot(h);
                 if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
                 h->slot_tile[size_t(sl)] = -1;
                 TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
-                TL_TRY(h, cudaEventRecord(t.ev[4][jg], h->h2d));
+                if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[4][jg], h->h2d));
                 TL_TRY(h, copy_w_tile(o, i, h->slot[sl], h->h2d));
-                TL_TRY(h, cudaEventRecord(t.ev[5][jg], h->h2d));
+                if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[5][jg], h->h2d));
                 TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
                 h->slot_tile[size_t(sl)] = g;
                 h2d_bytes += int64_t(tb);
@@ -940,7 +951,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
 
             // dW_i = X^T dY_i into staging slot gs (does not need W_i)
             TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gs], 0));
-            TL_TRY(h, cudaEventRecord(t.ev[0][jg], cs));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[0][jg], cs));
             tl::GemmDesc gw;
             gw.m_dim = s.K;
             gw.n_dim = s.Mi;
@@ -957,15 +968,15 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             gw.err = h->err_dev;
             if ((st = launch(h, gw, cs)) != TL_OK) return st;
             ++launches;
-            TL_TRY(h, cudaEventRecord(t.ev[1][jg], cs));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[1][jg], cs));
             TL_TRY(h, cudaEventRecord(h->ev_dwdone[gs], cs));
 
             // write dW_i back on the d2h stream
             if ((st = opt_wait(h, g, false)) != TL_OK) return st;
             TL_TRY(h, cudaStreamWaitEvent(h->d2h, h->ev_dwdone[gs], 0));
-            TL_TRY(h, cudaEventRecord(t.ev[6][jg], h->d2h));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[6][jg], h->d2h));
             TL_TRY(h, copy_dw_tile(o, i, h->stage[gs], h->d2h));
-            TL_TRY(h, cudaEventRecord(t.ev[7][jg], h->d2h));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[7][jg], h->d2h));
             if (h->opt) {
                 TL_TRY(h, cudaEventRecord(h->opt_ev_dw[size_t(g)], h->d2h));
                 h->opt_order.push_back(g);
@@ -976,8 +987,8 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             if (int(pend.size()) + 1 < gsz && j + 1 < s.N) {
                 // not the group's last (lowest) tile: its dX waits for the group
                 pend.push_back(sl);
-                TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
-                TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
+                if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
+                if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
                 continue;
             }
             // dX (+)= sum over the group's tiles i, i+1, .. of dY_i W_i^T, fp32;
@@ -985,7 +996,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             std::vector<int> grp(pend.rbegin(), pend.rend());  // ascending tile order from i+1
             grp.insert(grp.begin(), sl);                        // tile i first
             for (int gsl : grp) TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_ready[gsl], 0));
-            TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
             tl::GemmDesc gx;
             gx.m_dim = T;
             gx.n_dim = s.K;
@@ -1009,7 +1020,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             if ((st = launch(h, gx, cs)) != TL_OK) return st;
             ++dx_launches;
             ++launches;
-            TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
+            if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
             for (int psl : pend) {
                 TL_TRY(h, cudaEventRecord(h->ev_free[psl], cs));
                 h->slot_q.push_back(psl);
@@ -1312,6 +1323,9 @@ tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {
     out->sum_bwd_d2h_ms = h->bwd.sum_d2h;
     out->sum_bwd_gemm_ms = h->bwd.sum_gemm1 + h->bwd.sum_gemm2;
     out->persistent = h->persistent ? 1 : 0;
+    out->fwd_timed_calls = h->fwd.sum_timed;
+    out->bwd_timed_calls = h->bwd.sum_timed;
+    out->timing_every = h->timing_every;
     int32_t word = 0;
     TL_TRY(h, cudaMemcpy(&word, h->err_dev, sizeof(word), cudaMemcpyDeviceToHost));
     if (word != 0)
@@ -1471,6 +1485,14 @@ tl_status tiled_linear_set_tile_reuse(tl_handle* h, int32_t enable) {
     return TL_OK;
 }
 
+tl_status tiled_linear_set_timing(tl_handle* h, int32_t every) {
+    tl_status st = check_usable(h);
+    if (st != TL_OK) return st;
+    if (every < 1) return fail(h, TL_ERR_INVALID, "every must be >= 1");
+    h->timing_every = every;
+    return TL_OK;
+}
+
 tl_status tiled_linear_reset_stats(tl_handle* h) {
     if (!h) return TL_ERR_INVALID;
     DeviceGuard guard(h->device);
@@ -1479,6 +1501,7 @@ tl_status tiled_linear_reset_stats(tl_handle* h) {
     if (st != TL_OK) return st;
     for (Phase* p : {&h->fwd, &h->bwd}) {
         p->sum_calls = 0;
+        p->sum_timed = 0;
         p->sum_total = p->sum_gemm1 = p->sum_gemm2 = p->sum_h2d = p->sum_d2h = 0;
     }
     return TL_OK;

@@ -45,6 +45,7 @@ class tl_stats(ctypes.Structure):
         ("sum_bwd_h2d_ms", ctypes.c_double), ("sum_bwd_d2h_ms", ctypes.c_double),
         ("sum_bwd_gemm_ms", ctypes.c_double), ("bwd_gemm_ms", ctypes.c_float), ("persistent", ctypes.c_int32),
         ("bwd_reused_tiles", ctypes.c_int32),
+        ("fwd_timed_calls", ctypes.c_int64), ("bwd_timed_calls", ctypes.c_int64), ("timing_every", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -97,6 +98,8 @@ def load():
         L.tiled_linear_reset_stats.restype = st
         L.tiled_linear_set_tile_reuse.argtypes = [vp, i32]
         L.tiled_linear_set_tile_reuse.restype = st
+        L.tiled_linear_set_timing.argtypes = [vp, i32]
+        L.tiled_linear_set_timing.restype = st
         L.tiled_linear_adam_update.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, vp]
         L.tiled_linear_adam_update.restype = st
         L.tiled_linear_optimizer_create.argtypes = [ctypes.POINTER(vp), vp, vp, vp, vp, vp, vp]
@@ -189,6 +192,10 @@ def tiled_linear_get_stats(h: int) -> dict:
 
 def tiled_linear_reset_stats(h: int) -> None:
     _check(load().tiled_linear_reset_stats(h), "tiled_linear_reset_stats", h)
+
+
+def tiled_linear_set_timing(h: int, every: int) -> None:
+    _check(load().tiled_linear_set_timing(h, int(every)), "tiled_linear_set_timing", h)
 
 
 def tiled_linear_set_tile_reuse(h: int, enable: bool) -> None:
@@ -411,6 +418,10 @@ class TiledLinear:
         """Let backward calls take the tiles still resident from the calls
         before them (W must not change in between)."""
         tiled_linear_set_tile_reuse(self.handle, enable)
+
+    def set_timing(self, every: int) -> None:
+        """Record per-launch / per-copy timing events on every `every`-th call."""
+        tiled_linear_set_timing(self.handle, every)
 
     def close(self) -> int:
         st = TL_OK

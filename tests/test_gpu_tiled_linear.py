@@ -328,3 +328,30 @@ def test_tile_reuse_needs_per_tile_mode(tl):
     assert op.close() == tl.TL_OK
     w.close()
     dw.close()
+
+
+def test_sampled_timing_counts_and_results(tl):
+    """Timing every third call: all calls counted, three of seven timed, the
+    results unchanged."""
+    T, K, M, N = 128, 512, 2048, 4
+    ref = run_op(tl, T, K, M, N, 1, seed=3, calls=1, persistent=False)
+    w, dw = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
+    I.fill_w_host(w.tensor, K, M, N, True, 3)
+    op = make_op(tl, K, M, N, 1, w, dw, persistent=False)
+    op.set_timing(3)
+    xd, dyd = ref.x.cuda(), ref.dy.cuda()
+    for _ in range(7):
+        y = op.forward(xd)
+        dx = op.backward(xd, dyd)
+    torch.cuda.synchronize()
+    st = op.stats()
+    assert st["fwd_calls"] == 7 and st["bwd_calls"] == 7
+    assert st["fwd_timed_calls"] == 3 and st["bwd_timed_calls"] == 3 and st["timing_every"] == 3
+    assert st["fwd_gemm_ms"] > 0 and st["sum_fwd_gemm_ms"] > 0
+    assert _same(y.cpu(), ref.y) and _same(dx.cpu(), ref.dx)
+    with pytest.raises(tl.TiledLinearError) as ei:
+        op.set_timing(0)
+    assert ei.value.status == tl.TL_ERR_INVALID
+    assert op.close() == tl.TL_OK
+    w.close()
+    dw.close()
