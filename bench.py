@@ -706,6 +706,10 @@ def run_ours(args, cfg, dist: Dist):
         # against the timed calls' own spans (timing adds a little to them)
         "compute_stream_idle_pct": round(100.0 * max(0.0, 1.0 - gemm_ms / max(
             st["sum_fwd_total_ms"] + st["sum_bwd_total_ms"], 1e-9)), 2),
+        "fwd_idle_ms_per_step": round(max(0.0, st["sum_fwd_total_ms"] - st["sum_fwd_gemm_ms"]) / max(fc, 1), 4),
+        "bwd_idle_ms_per_step": round(max(0.0, st["sum_bwd_total_ms"] - st["sum_bwd_gemm_ms"]) / max(bc, 1), 4),
+        "fwd_h2d_gbs_per_copy": round(st["fwd_h2d_bytes"] * fc / (st["sum_fwd_h2d_ms"] / 1e3) / 1e9, 1)
+        if st["sum_fwd_h2d_ms"] > 0 else None,
         "h2d_gbs_per_copy": round((st["fwd_h2d_bytes"] + st["bwd_h2d_bytes"]) * fc / (h2d_ms / 1e3) / 1e9, 1)
         if h2d_ms > 0 else None,
         "d2h_gbs_per_copy": round(st["bwd_d2h_bytes"] * bc / (st["sum_bwd_d2h_ms"] / 1e3) / 1e9, 1)

@@ -408,16 +408,33 @@ void end_call(Phase& p, CallSlot& c) {
 void reset_ring(tl_handle* h) {
     h->slot_q.clear();
     for (int s = 0; s <= h->d; ++s) h->slot_q.push_back(s);
-    h->slot_tile.assign(size_t(h->slot_cap), -1);
+    h->slot_tile.assign(h->slot.size(), -1);
+}
+
+// The dW staging slots double as weight slots for the forward, where they sit
+// idle: slot index slot_cap + g is staging slot g.  A backward takes them out
+// of the free queue (its dW GEMMs write them) and hands them back once their
+// last write-back has left.
+int staging_slot(const tl_handle* h, int g) { return h->slot_cap + g; }
+
+void withdraw_staging(tl_handle* h) {
+    std::deque<int> q;
+    for (int sl : h->slot_q)
+        if (sl < h->slot_cap) q.push_back(sl);
+    h->slot_q.swap(q);
+    for (int g = 0; g < h->nstage; ++g) h->slot_tile[size_t(staging_slot(h, g))] = -1;
 }
 
 // The slot for the next fetch: the one whose last reader was enqueued
 // earliest (the fetch waits for that reader on the h2d stream).
-int take_slot(tl_handle* h) {
-    if (h->slot_q.empty()) return -1;
-    const int sl = h->slot_q.front();
-    h->slot_q.pop_front();
-    return sl;
+int take_slot(tl_handle* h, bool ring_only = false) {
+    for (auto it = h->slot_q.begin(); it != h->slot_q.end(); ++it)
+        if (!ring_only || *it < h->slot_cap) {
+            const int sl = *it;
+            h->slot_q.erase(it);
+            return sl;
+        }
+    return -1;
 }
 
 // With a host optimizer attached: the host waits before it queues a copy that
@@ -457,7 +474,7 @@ tl_status finish_auto_depth(tl_handle* h) {
                                         reinterpret_cast<CUdeviceptr>(h->flags + tl::kFlagFreed + s),
                                         uint32_t(h->fetch_seq), kWriteDefault));
         } else {
-            for (int s = 0; s < h->slot_cap; ++s) TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[s], 0));
+            for (size_t s = 0; s < h->slot.size(); ++s) TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[s], 0));
             h->fetch_seq = 0;
         }
         h->d = dnew;
@@ -635,8 +652,9 @@ tl_status create_ops(tl_handle** out, std::vector<Op> ops, int32_t d, void* ws, 
     h->tile_counter = reinterpret_cast<uint32_t*>(h->ws + kTileCounterOffset);
     uint8_t* p = h->ws + kHeaderBytes;
     for (int s = 0; s < h->slot_cap; ++s, p += tb) h->slot.push_back(p);
-    reset_ring(h);
     for (int g = 0; g < h->nstage; ++g, p += tb) h->stage.push_back(p);
+    for (int g = 0; g < h->nstage; ++g) h->slot.push_back(h->stage[size_t(g)]);  // see staging_slot
+    reset_ring(h);
 
     if (cudaMemset(h->ws, 0, kHeaderBytes) != cudaSuccess ||
         cudaHostAlloc(reinterpret_cast<void**>(&h->err_mirror), sizeof(int32_t), cudaHostAllocPortable) !=
@@ -656,7 +674,8 @@ tl_status create_ops(tl_handle** out, std::vector<Op> ops, int32_t d, void* ws, 
             if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
         return true;
     };
-    if (!mk(h->ev_ready, h->slot_cap) || !mk(h->ev_free, h->slot_cap) || !mk(h->ev_dwdone, h->nstage) ||
+    const int nbuf = h->slot_cap + h->nstage;
+    if (!mk(h->ev_ready, nbuf) || !mk(h->ev_free, nbuf) || !mk(h->ev_dwdone, h->nstage) ||
         !mk(h->ev_drained, h->nstage)) {
         h->msg = std::string("event creation: ") + cudaGetErrorString(cudaGetLastError());
         return bail(TL_ERR_CUDA);
@@ -811,7 +830,9 @@ tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys,
         for (int i = 0; i < s.N; ++i) {
             const int g = o.first + i;  // tile index in the handle's order
             if ((st = opt_wait(h, g, true)) != TL_OK) return st;
-            const int sl = take_slot(h);
+            // the pass's last d+1 tiles go to ring slots: a backward that
+            // follows may take them from there (tile reuse)
+            const int sl = take_slot(h, g >= h->n_total - (h->d + 1));
             if (sl < 0) return fail(h, TL_ERR_STATE, "internal: no ring slot to fetch into");
             h->slot_tile[size_t(sl)] = -1;
             TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
@@ -864,11 +885,13 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
                          float* dx, float* scr_dx, void* scr_dy, cudaStream_t cs) {
     tl_status st;
     const int L = int(h->ops.size());
+    withdraw_staging(h);
     if (T == 0) {  // dW = X^T dY over an empty sum: zero
         if (h->opt) h->opt_order.clear();
         for (int l = L - 1; l >= 0; --l) {
             const Op& o = h->ops[size_t(l)];
             TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[0], 0));
+            TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_free[staging_slot(h, 0)], 0));
             TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tile_bytes(o.s.K, o.s.Mi), cs));
             for (int i = o.s.N - 1; i >= 0; --i) {
                 const int g = o.first + i;
@@ -883,6 +906,10 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             TL_TRY(h, cudaEventRecord(h->ev_drained[0], cs));
         }
         if (h->opt) h->opt_have_bwd = true;
+        for (int g = 0; g < h->nstage; ++g) {
+            TL_TRY(h, cudaEventRecord(h->ev_free[staging_slot(h, g)], cs));
+            h->slot_q.push_back(staging_slot(h, g));
+        }
         return TL_OK;
     }
     CallSlot* tp = begin_call(h, h->bwd, &st);
@@ -909,6 +936,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
     int64_t h2d_bytes = 0, d2h_bytes = 0;
     int launches = 0;
     int jg = 0;  // position in the backward's tile order
+    std::vector<bool> stage_ready(size_t(h->nstage), false);  // forward done with the staging slot
     if (h->opt) h->opt_order.clear();
     TL_TRY(h, cudaEventRecord(t.start, cs));
     for (int l = L - 1; l >= 0; --l) {
@@ -951,6 +979,10 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
 
             // dW_i = X^T dY_i into staging slot gs (does not need W_i)
             TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_drained[gs], 0));
+            if (!stage_ready[size_t(gs)]) {  // the forward may have read a weight tile from it
+                TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_free[staging_slot(h, gs)], 0));
+                stage_ready[size_t(gs)] = true;
+            }
             if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[0][jg], cs));
             tl::GemmDesc gw;
             gw.m_dim = s.K;
@@ -983,6 +1015,12 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             }
             TL_TRY(h, cudaEventRecord(h->ev_drained[gs], h->d2h));
             d2h_bytes += int64_t(tb);
+            if (jg >= NT - h->nstage) {
+                // the staging slot's last write-back of this call: from here
+                // it serves the next forward (in release order in the queue)
+                TL_TRY(h, cudaEventRecord(h->ev_free[staging_slot(h, gs)], h->d2h));
+                h->slot_q.push_back(staging_slot(h, gs));
+            }
 
             if (int(pend.size()) + 1 < gsz && j + 1 < s.N) {
                 // not the group's last (lowest) tile: its dX waits for the group
