@@ -622,16 +622,19 @@ def run_ours(args, cfg, dist: Dist):
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.25)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for _ in range(args.steps):
+    # one event per step boundary as well (the step-time distribution shows
+    # whether a slow average comes from a few stalled steps)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    marks[0].record(s)
+    for k in range(args.steps):
         op.forward(x, y, stream=s)
         op.backward(x, dy, dx, stream=s)
-    e1.record(s)
+        marks[k + 1].record(s)
     torch.cuda.synchronize()
     dist.barrier()
     clocks = sampler.stop()
-    ms_local = e0.elapsed_time(e1) / args.steps
+    ms_local = marks[0].elapsed_time(marks[-1]) / args.steps
+    per_step = sorted(marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps))
     ms = dist.max(ms_local)
     st = op.stats()
     persistent = bool(st.get("persistent", 0))
@@ -702,6 +705,9 @@ def run_ours(args, cfg, dist: Dist):
         gemm_ms = st["sum_fwd_gemm_ms"] + st["sum_bwd_gemm_ms"]
     h2d_ms = st["sum_fwd_h2d_ms"] + st["sum_bwd_h2d_ms"]
     out["timed_region"] = {
+        "step_ms_median": round(per_step[len(per_step) // 2], 4),
+        "step_ms_p90": round(per_step[min(len(per_step) - 1, int(0.9 * len(per_step)))], 4),
+        "step_ms_max": round(per_step[-1], 4),
         "gemm_ms_per_step": round(gemm_ms / max(fc, 1), 4),
         # against the timed calls' own spans (timing adds a little to them)
         "compute_stream_idle_pct": round(100.0 * max(0.0, 1.0 - gemm_ms / max(
