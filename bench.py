@@ -47,6 +47,9 @@ CONFIGS = {
     "1t": dict(T=4096, K=25600, M=102400, N=16, d=2,
                workload="1T-width FFN: X bf16 [4096,25600], W bf16 [25600,102400] (5.2 GB) pinned host, "
                         "N=16 tiles of 6400 cols, d=2"),
+    "sweep": dict(T=8192, K=16384, M=65536, N=16, d=2,
+                  workload="ait sweep: X bf16 [T,16384], W bf16 [16384,65536] (2 GiB) pinned host (tile-major), "
+                           "N=16 tiles of 4096 cols, dY ~N(0,1)"),
     "64k": dict(T=2048, K=65536, M=262144, N=16, d=2,
                 workload="64K-hidden FFN: X bf16 [2048,65536], W bf16 [65536,262144] (32 GiB + 32 GiB dW) "
                          "pinned host, N=16 tiles of 16384 cols, d=2"),
@@ -811,6 +814,97 @@ def run_ours(args, cfg, dist: Dist):
     return out
 
 
+SWEEP_T = [512 << j for j in range(8)]  # 512 ... 65536
+SWEEP_D = [1, 2, 3, 4]
+
+
+def run_sweep(args, dist: Dist):
+    """The arithmetic-intensity sweep: one streamed layer (K = 16384,
+    M = 65536, N = 16) timed at T = 512 ... 65536 tokens and depth d = 1 ... 4.
+    Per point: TFLOP/s over the fwd+bwd step, the step roofline
+    max(6TKM/R, 4KM/B_h2d, 2KM/B_d2h) with the link measured here, and the
+    exposed copy against the same GEMMs on resident W and the same copies
+    alone.  The link hides behind compute once ait = 1.5 T FLOP/B passes
+    R / B_h2d (memory-centric tiling, "The honest cost")."""
+    import torch
+
+    import __graft_entry__ as g
+    from offload_streamed_gb300 import tiled_linear as tl
+
+    torch.cuda.set_device(dist.local_rank)
+    g.build()
+    peaks = load_peaks()
+    cfg = dict(CONFIGS["sweep"])
+    cfg["T"] = max(SWEEP_T)
+    K, M, N = cfg["K"], cfg["M"], cfg["N"]
+    Mi = M // N
+    log(f"[sweep] building workload (T up to {cfg['T']}, K={K}, M={M}, N={N})")
+    w, dw, x_all, dy_all, _ = make_workload(cfg, args.seed, "cuda", need_host_w_rowmajor=False)
+    y_all = torch.empty(cfg["T"], M, dtype=torch.bfloat16, device="cuda")
+    dx_all = torch.empty(cfg["T"], K, dtype=torch.float32, device="cuda")
+    link = measure_link(w, dw, 1 << 30)
+    t_copy = time_copy_schedule(cfg, w, dw)
+    w_dev = w.tensor.view(N, K, Mi).to("cuda").permute(1, 0, 2).reshape(K, M).contiguous()
+    R = peaks["bf16_tflops"] * 1e12
+    bh, bd = link["h2d_gbs"] * 1e9, link["d2h_gbs"] * 1e9
+    s = torch.cuda.current_stream()
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dist.local_rank).uuid)
+        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    resident = {}
+    points = []
+    for d in SWEEP_D:
+        op = tl.TiledLinear(K, M, N, d, w, dw, tile_major=True)
+        for T in SWEEP_T:
+            flops = 6.0 * T * K * M
+            t_roof = max(flops / R, 4.0 * K * M / bh, 2.0 * K * M / bd)
+            steps = max(3, min(20, int(1.5 / t_roof)))
+            x, dy, y, dx = x_all[:T], dy_all[:T], y_all[:T], dx_all[:T]
+            c = dict(cfg, T=T, d=d)
+            key = (T, dx_group(d, N, Mi))
+            if key not in resident:
+                resident[key] = time_resident_compute(tl, c, x, dy, w_dev, steps)
+            for _ in range(2):
+                op.forward(x, y, stream=s)
+                op.backward(x, dy, dx, stream=s)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(steps):
+                op.forward(x, y, stream=s)
+                op.backward(x, dy, dx, stream=s)
+            e1.record(s)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / steps
+            t_res = resident[key]
+            points.append({"T": T, "d": d, "steps": steps, "ms_per_step": round(ms, 3),
+                           "tflops": round(flops / (ms / 1e3) / 1e12, 1),
+                           "roofline_tflops": round(flops / t_roof / 1e12, 1),
+                           "frac": round(t_roof * 1e3 / ms, 4),
+                           "bound_by": ["tensor", "h2d", "d2h"][
+                               [flops / R, 4.0 * K * M / bh, 2.0 * K * M / bd].index(t_roof)],
+                           "ait_h2d_flop_per_byte": 1.5 * T,
+                           "t_compute_resident_ms": round(t_res, 3),
+                           "resident_tflops": round(flops / (t_res / 1e3) / 1e12, 1),
+                           "exposed_copy_pct": round(100.0 * max(0.0, ms - t_res) / t_copy, 2)})
+            log(f"[sweep] {points[-1]}")
+        assert op.close() == tl.TL_OK
+    clocks = sampler.stop()
+    del w_dev
+    w.close()
+    dw.close()
+    return {"sweep": "ait", "metric": METRIC, "unit": UNIT, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg["workload"], "K": K, "M": M, "N": N, "T": SWEEP_T, "d": SWEEP_D,
+                       "host_layout": "tile-major [N][K][M/N]"},
+            "link": {k: round(v, 1) if isinstance(v, float) else v for k, v in link.items()},
+            "R_tflops": peaks["bf16_tflops"], "crossover_T": round(R / (1.5 * bh)),
+            "t_copy_only_ms": round(t_copy, 3), "points": points, "clocks": clocks}
+
+
 def run_reference(args, cfg, dist: Dist):
     """The oracle, as it stands, timed on the host cores: each step is the
     full forward + backward of the first `tokens` tokens of the workload."""
@@ -862,6 +956,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the arithmetic-intensity sweep (K=16384, M=65536, N=16; T = 512..65536, "
+                         "d = 1..4) and print one JSON line with every point")
     ap.add_argument("--profile-gemms", type=int, default=0, metavar="R",
                     help="only run the three resident GEMMs of one tile R times (for ncu), print nothing")
     args = ap.parse_args()
@@ -875,6 +972,10 @@ def main():
         cfg["workload"] += f" (T overridden to {args.T})"
     if args.profile_gemms > 0:
         profile_gemms(cfg, args.profile_gemms)
+        return
+    if args.sweep:
+        out = run_sweep(args, Dist("nccl"))
+        print(json.dumps(out), flush=True)
         return
     if args.impl == "reference":
         # rank 0 alone times the CPU oracle; other ranks have nothing to do
