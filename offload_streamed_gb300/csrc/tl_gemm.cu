@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const __grid_constant__ CUtensorMap map_d, const __grid_constant__ BSegMaps segs,
                 const KParams p) {
-    using G = Geo<PAIR, OUT_F32 ? 0 : 2>;
+    using G = Geo<PAIR, 2>;
     const WaitCtx wc{p.err, p.timeout_ns};
     constexpr int S = G::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -266,13 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kFirstEpilogueWarp) {
         // ---------------- epilogue (each CTA stores its own 128 rows) ----------------
-        // bf16 outputs leave through TMA stores of swizzled staging boxes; fp32
-        // outputs (dX, possibly accumulated) are written by the threads
-        // directly, which keeps shared-memory bandwidth for the tensor cores.
+        // Outputs leave through swizzled staging boxes in shared memory: TMA
+        // stores for bf16 and for a first fp32 dX, TMA reduce-adds (the add
+        // done in L2) for an accumulated one.
         constexpr int kChunk = OUT_F32 ? 32 : 64;
         const int q = warp & 3;
         const uint32_t epi0 = smem0 + S * G::kStageBytes + uint32_t(q) * 2u * kEpiBuf;
-        if (!OUT_F32 && lane == 0) tma_prefetch_map(&map_d);
+        if (lane == 0) tma_prefetch_map(&map_d);
         uint32_t buf = 0;
         for (int it = 0;; ++it) {
             int tile;
@@ -297,9 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * kBlockN;
             if constexpr (OUT_F32) {
-                const int64_t row = int64_t(row0) + lane;
-                epi_f32_direct(static_cast<float*>(p.d) + row * p.ldd + n0, row < p.m_dim, p.n_dim - n0, t_row,
-                               nchunks, p.accumulate != 0);
+                epi_f32_tma(&map_d, t_row, epi0, buf, nchunks, n0, row0, lane, p.accumulate != 0);
             } else {
                 epi_bf16_tma(&map_d, t_row, epi0, buf, nchunks, n0, row0, lane);
             }
@@ -310,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else mbar_arrive(tempty_bar(acc));
             }
         }
-        if (!OUT_F32 && lane == 0) bulk_wait_group_all();  // stores complete before the CTA exits
+        if (lane == 0) bulk_wait_group_all();  // stores complete before the CTA exits
         __syncwarp();
     }
 
@@ -372,7 +370,7 @@ template <bool A_MN, bool B_MN, bool OUT_F32, bool PAIR>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const BSegMaps& segs,
                        const KParams& kp, int grid, cudaStream_t stream) {
     auto kern = gemm_kernel<A_MN, B_MN, OUT_F32, PAIR>;
-    constexpr size_t smem = Geo<PAIR, OUT_F32 ? 0 : 2>::kSmem;
+    constexpr size_t smem = Geo<PAIR, 2>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};

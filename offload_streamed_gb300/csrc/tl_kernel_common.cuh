@@ -35,8 +35,7 @@ struct Geo {
     static constexpr uint32_t kStageB = uint32_t(kBRows) * kBlockK * 2;
     static constexpr uint32_t kStageBytes = kStageA + kStageB;
     static constexpr uint32_t kEpiBytes = 4u * EPI_BOXES * kEpiBuf;
-    // 6 stages in pair mode: a 7th (room for it exists with fp32 outputs,
-    // which need no staging boxes) measured 0.6 % slower on the dX GEMM
+    // 6 stages in pair mode, with the epilogue's staging boxes beside them
     static constexpr int kStages = PAIR ? 6 : 4;
     static constexpr size_t kSmem = size_t(kStages) * kStageBytes + kEpiBytes + kBarBytes + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -175,70 +174,36 @@ __device__ __forceinline__ void epi_bf16_tma(const CUtensorMap* map, uint32_t t_
     }
 }
 
-// fp32: per 32-column chunk, tcgen05.ld and a direct 128-byte store of the
-// lane's row at out_row + 32c (columns past `rem0` are skipped); with `rmw`
-// the old values are added, the next chunk's loaded while this one is
-// added and stored.
-__device__ __forceinline__ void epi_f32_direct(float* out_row, bool row_ok, int rem0, uint32_t t_row, int nchunks,
-                                               bool rmw) {
-    // The output streams through L2 once per launch (read and written back):
-    // evict it first, so that it does not push out the operand blocks the
-    // tile order keeps resident.
+// fp32 through TMA: per 32-column chunk, tcgen05.ld of the lane's row into a
+// 128B-swizzled staging box (two per warp, alternating), and lane 0 issues a
+// TMA store of the 32 x 32 box at (col0 + 32c, row0) -- or, with `add`, a TMA
+// reduce-add of it into the values there, so that the read-modify-write
+// happens in L2 on whole lines instead of as per-thread loads and stores.
+__device__ __forceinline__ void epi_f32_tma(const CUtensorMap* map, uint32_t t_row, uint32_t epi0, uint32_t& buf,
+                                            int nchunks, int col0, int row0, int lane, bool add) {
+    // The output streams through L2 once per launch: evict it first, so that
+    // it does not push out the operand blocks the tile order keeps resident.
     const uint64_t pol = l2_policy_evict_first();
-    auto load_old = [&](int c, float4(&dst)[8]) {
-        const float* src = out_row + c * 32;
-        const int rem = rem0 - c * 32;
-        if (row_ok && rem >= 32) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = ld_global_v4_hint(src + 4 * j, pol);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                dst[j].x = (row_ok && 4 * j + 0 < rem) ? src[4 * j + 0] : 0.f;
-                dst[j].y = (row_ok && 4 * j + 1 < rem) ? src[4 * j + 1] : 0.f;
-                dst[j].z = (row_ok && 4 * j + 2 < rem) ? src[4 * j + 2] : 0.f;
-                dst[j].w = (row_ok && 4 * j + 3 < rem) ? src[4 * j + 3] : 0.f;
-            }
-        }
-    };
-    float4 old[8];
-    if (rmw && nchunks > 0) load_old(0, old);
     for (int c = 0; c < nchunks; ++c) {
-        uint32_t w[32];
-        tmem_ld_32cols(t_row + uint32_t(c) * 32u, w);
-        float4 nxt[8];
-        if (rmw && c + 1 < nchunks) load_old(c + 1, nxt);
+        uint32_t v[32];
+        tmem_ld_32cols(t_row + uint32_t(c) * 32u, v);
         tmem_ld_wait();
-        float4 val[8];
+        const uint32_t sbuf = epi0 + buf * kEpiBuf;
+        if (lane == 0) bulk_wait_group_read<1>();  // the copy that last used sbuf has read it
+        __syncwarp();
+        const uint32_t row_addr = sbuf + uint32_t(lane) * 128u;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            val[j] = make_float4(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]),
-                                 __uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]));
-            if (rmw) {
-                val[j].x = old[j].x + val[j].x;
-                val[j].y = old[j].y + val[j].y;
-                val[j].z = old[j].z + val[j].z;
-                val[j].w = old[j].w + val[j].w;
-            }
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(row_addr + ((uint32_t(j) ^ (uint32_t(lane) & 7u)) << 4), v[4 * j], v[4 * j + 1],
+                         v[4 * j + 2], v[4 * j + 3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            if (add) tma_reduce_add_2d_hint(map, sbuf, col0 + c * 32, row0, pol);
+            else tma_store_2d_hint(map, sbuf, col0 + c * 32, row0, pol);
+            bulk_commit_group();
         }
-        float* dst = out_row + c * 32;
-        const int rem = rem0 - c * 32;
-        if (row_ok && rem >= 32) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) st_global_v4_hint(dst + 4 * j, val[j], pol);
-        } else if (row_ok) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (4 * j + 0 < rem) dst[4 * j + 0] = val[j].x;
-                if (4 * j + 1 < rem) dst[4 * j + 1] = val[j].y;
-                if (4 * j + 2 < rem) dst[4 * j + 2] = val[j].z;
-                if (4 * j + 3 < rem) dst[4 * j + 3] = val[j].w;
-            }
-        }
-        if (rmw && c + 1 < nchunks) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) old[j] = nxt[j];
-        }
+        buf ^= 1u;
     }
 }
 

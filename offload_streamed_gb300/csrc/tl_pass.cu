@@ -50,6 +50,7 @@ struct PassMaps {
     CUtensorMap b1;                    // bwd: dY [T,M] N-major (B of dW)
     CUtensorMap stage[kMaxPassStages]; // bwd: dW staging slots [K, Mi] bf16 store
     CUtensorMap w[kMaxPassSlots];      // ring slots [K, Mi]: fwd N-major (B of Y); bwd K-major (B of dX)
+    CUtensorMap dx;                    // bwd: dX [T, K] fp32 store / reduce-add
 };
 
 // Job kind 0: the GEMM that reads W (fwd Y_i, bwd dX); kind 1: bwd dW_i.
@@ -64,8 +65,6 @@ struct PassParams {
     uint32_t* done;
     uint32_t* dwdone;
     uint32_t* dxdone;
-    float* dx;
-    int64_t ldx;
     int32_t* err;
     uint64_t timeout_ns, flag_timeout_ns;
 };
@@ -315,9 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) pass_kernel(const __grid_constant
             }
             if (BWD && kind == 0 && b.G > 0) {  // dX of the previous group fully stored
                 int okw = 1;
-                if (lane == 0)
+                if (lane == 0) {
                     okw = poll_geq(p.dxdone + (b.G - 1), uint32_t(kParts * p.tiles[0]), wc, kErrFlagWait,
                                    p.flag_timeout_ns);
+                    fence_proxy_async_global();  // before this lane's TMA reduce-adds of the same dX
+                }
                 okw = __shfl_sync(0xffffffffu, okw, 0);
                 if (!okw) break;
             }
@@ -346,13 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1) pass_kernel(const __grid_constant
                         st_release_u32(p.flags + kFlagDwReady + g, sj + 1u);
                 }
             } else {
-                const int64_t row = int64_t(row0) + lane;
-                epi_f32_direct(p.dx + row * p.ldx + n0, row < p.m_dim[0], p.n_dim[0] - n0, t_row, nchunks, b.G > 0);
-                __syncwarp();
+                epi_f32_tma(&maps.dx, t_row, epi0, buf, nchunks, n0, row0, lane, b.G > 0);
                 if (lane == 0) {
+                    bulk_wait_group_all();  // this warp's part of the dX tile is in global memory
+                    fence_proxy_async_global();
                     __threadfence();
                     atomicAdd(p.dxdone + b.G, 1u);
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -463,6 +465,7 @@ cudaError_t pass_launch(const PassDesc& d, int num_sms, cudaStream_t stream, std
         for (int g = 0; g < d.nstage; ++g) ok = ok && make_tensor_map(&maps.stage[g], d.stages[g], Mi, K, Mi, 32, false, why);
         for (int s = 0; s < d.nslots; ++s)
             ok = ok && make_tensor_map(&maps.w[s], d.slots[s], Mi, K, Mi, kBlockN / 2, false, why);
+        ok = ok && make_tensor_map(&maps.dx, d.dx, K, T, K, 32, true, why);
         set_kind(pp, 0, T, K, Mi);  // dX (per pass position; a job spans its group)
         set_kind(pp, 1, K, Mi, T);  // dW
         pp.jobs_per_tile = pp.tiles[0] + pp.tiles[1];
@@ -487,8 +490,6 @@ cudaError_t pass_launch(const PassDesc& d, int num_sms, cudaStream_t stream, std
     pp.done = d.done;
     pp.dwdone = d.dwdone;
     pp.dxdone = d.dxdone;
-    pp.dx = d.dx;
-    pp.ldx = K;
     pp.err = d.err;
     pp.timeout_ns = d.timeout_ns;
     pp.flag_timeout_ns = d.flag_timeout_ns;

@@ -99,6 +99,39 @@ def test_gemm_dx_store_then_accumulate(tl, T, K, n):
     assert np.array_equal(dx.cpu().numpy(), first + first)
 
 
+def test_gemm_dx_accumulate_is_an_fp32_add(tl):
+    """dX (+)= dY . W^T adds each new value to the old one as one IEEE fp32
+    addition: round to nearest, ties to even, subnormals kept.  dY selects
+    one column of W per row, so every new value is a single exact product;
+    the old values are chosen so that the sums hit ties at 2^24 and land on
+    or start from subnormals."""
+    T, K, n = 256, 64, 64
+    rng = np.random.default_rng(3)
+    dy = torch.zeros(T, n, dtype=torch.float32)
+    dy[torch.arange(T), torch.arange(T) % n] = 1.0
+    w = torch.tensor(rng.integers(-8, 9, size=(K, n)), dtype=torch.float32)
+    w[0], w[1], w[2], w[3] = 1.0, 3.0, 0.0, -(2.0 ** -126)
+    old = rng.integers(-100, 101, size=(T, K)).astype(np.float32)
+    old[:, 0] = old[:, 1] = np.float32(2.0 ** 24)   # + 1 and + 3: ties, to even
+    old[:, 2] = np.float32(2.0 ** -130)             # + 0: a subnormal survives
+    old[:, 3] = np.float32(1.5 * 2.0 ** -126)       # - 2^-126: a subnormal result
+    dyb, wb = dy.bfloat16(), w.bfloat16()
+    assert torch.equal(wb.float(), w) and torch.equal(dyb.float(), dy)
+    dyd, wd = _dev(dyb), _dev(wb)
+    dx = torch.from_numpy(old.copy()).cuda()
+    err = _err_word()
+    st = torch.cuda.current_stream().cuda_stream
+    tl.tiled_linear_gemm_dx(T, K, n, dyd.data_ptr(), n, wd.data_ptr(), n, dx.data_ptr(), K, 1, err.data_ptr(), st)
+    torch.cuda.synchronize()
+    assert int(err[0].item()) == 0
+    new = w.numpy()[:, np.arange(T) % n].T.astype(np.float32)  # [T, K]: the one product of each entry
+    want = old + new  # numpy: IEEE fp32 addition
+    got = dx.cpu().numpy()
+    assert want[0, 0] == np.float32(2.0 ** 24) and want[0, 1] == np.float32(2.0 ** 24 + 4)
+    assert want[0, 3] == np.float32(2.0 ** -127) and want[0, 2] == np.float32(2.0 ** -130)
+    assert np.array_equal(got.view(np.int32), want.view(np.int32))
+
+
 def test_gemm_integer_exact(tl):
     """Entries in {-1, 0, 1}: every partial sum is a small integer, exact in
     fp32 and (|values| <= 256) in bf16, so the GPU must equal the integer
