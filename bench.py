@@ -187,12 +187,15 @@ def oracle_sample_run(xh, dyh, w_rowmajor_bits, T_s: int):
 
 
 def oracle_baseline(xh, dyh, w_rowmajor_bits, target_s: float = 12.0):
-    """Pick a token sample so that the timed oracle run takes ~target_s."""
-    K, M = w_rowmajor_bits.shape
-    T_s = 2
-    dt, fl, thr = oracle_sample_run(xh, dyh, w_rowmajor_bits, T_s)
-    rate = fl / max(dt, 1e-9)
-    T_s = max(2, min(xh.shape[0], int(target_s * rate / (6.0 * K * M))))
+    """Pick a token sample so that the timed oracle run takes ~target_s.  A
+    run costs a fixed part (dW is a full [K, M] output whatever the token
+    count) plus a part per token; two short runs fit both."""
+    t1, t2 = 2, 16
+    d1 = oracle_sample_run(xh, dyh, w_rowmajor_bits, t1)[0]
+    d2 = oracle_sample_run(xh, dyh, w_rowmajor_bits, t2)[0]
+    per_token = max((d2 - d1) / (t2 - t1), 1e-6)
+    fixed = max(d1 - per_token * t1, 0.0)
+    T_s = max(2, min(xh.shape[0], int((target_s - fixed) / per_token)))
     dt, fl, thr = oracle_sample_run(xh, dyh, w_rowmajor_bits, T_s)
     return {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
             "sample": f"full fwd+bwd (Y, dX, dW) for the first {T_s} tokens of the workload "
