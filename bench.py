@@ -828,7 +828,9 @@ def run_sweep(args, dist: Dist):
     max(6TKM/R, 4KM/B_h2d, 2KM/B_d2h) with the link measured here, and the
     exposed copy against the same GEMMs on resident W and the same copies
     alone.  The link hides behind compute once ait = 1.5 T FLOP/B passes
-    R / B_h2d (memory-centric tiling, "The honest cost")."""
+    R / B_h2d (memory-centric tiling, "The honest cost").  A point's rate,
+    fraction and exposed copy come from its median step, since the host link
+    stalls now and then for tens of milliseconds; the mean is reported too."""
     import torch
 
     import __graft_entry__ as g
@@ -858,7 +860,6 @@ def run_sweep(args, dist: Dist):
         gpu_id = None
     sampler = ClockSampler(gpu_id)
     sampler.start()
-    resident = {}
     points = []
     for d in SWEEP_D:
         op = tl.TiledLinear(K, M, N, d, w, dw, tile_major=True)
@@ -868,24 +869,27 @@ def run_sweep(args, dist: Dist):
             steps = max(3, min(20, int(1.5 / t_roof)))
             x, dy, y, dx = x_all[:T], dy_all[:T], y_all[:T], dx_all[:T]
             c = dict(cfg, T=T, d=d)
-            key = (T, dx_group(d, N, Mi))
-            if key not in resident:
-                resident[key] = time_resident_compute(tl, c, x, dy, w_dev, steps)
+            # resident GEMMs timed right before the streamed steps: the
+            # power-capped clock drifts by a few percent over minutes
+            t_res = time_resident_compute(tl, c, x, dy, w_dev, steps)
             for _ in range(2):
                 op.forward(x, y, stream=s)
                 op.backward(x, dy, dx, stream=s)
             torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(s)
-            for _ in range(steps):
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+            marks[0].record(s)
+            for k in range(steps):
                 op.forward(x, y, stream=s)
                 op.backward(x, dy, dx, stream=s)
-            e1.record(s)
+                marks[k + 1].record(s)
             torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / steps
-            t_res = resident[key]
-            points.append({"T": T, "d": d, "steps": steps, "ms_per_step": round(ms, 3),
+            mean = marks[0].elapsed_time(marks[-1]) / steps
+            per_step = sorted(marks[k].elapsed_time(marks[k + 1]) for k in range(steps))
+            ms = per_step[steps // 2]  # median: robust to the host link's occasional stalls
+            points.append({"T": T, "d": d, "steps": steps, "ms_per_step_median": round(ms, 3),
+                           "ms_per_step_mean": round(mean, 3), "ms_per_step_max": round(per_step[-1], 3),
                            "tflops": round(flops / (ms / 1e3) / 1e12, 1),
+                           "tflops_mean": round(flops / (mean / 1e3) / 1e12, 1),
                            "roofline_tflops": round(flops / t_roof / 1e12, 1),
                            "frac": round(t_roof * 1e3 / ms, 4),
                            "bound_by": ["tensor", "h2d", "d2h"][
