@@ -189,8 +189,10 @@ def oracle_sample_run(xh, dyh, w_rowmajor_bits, T_s: int):
 def oracle_baseline(xh, dyh, w_rowmajor_bits, target_s: float = 12.0):
     """Pick a token sample so that the timed oracle run takes ~target_s.  A
     run costs a fixed part (dW is a full [K, M] output whatever the token
-    count) plus a part per token; two short runs fit both."""
-    t1, t2 = 2, 16
+    count) plus a part per token; two short runs fit both, with at least 16
+    tokens each so that the forward and dX loops (parallel over tokens) keep
+    all cores busy as the final run does."""
+    t1, t2 = 16, 64
     d1 = oracle_sample_run(xh, dyh, w_rowmajor_bits, t1)[0]
     d2 = oracle_sample_run(xh, dyh, w_rowmajor_bits, t2)[0]
     per_token = max((d2 - d1) / (t2 - t1), 1e-6)
@@ -533,6 +535,109 @@ def run_host_adam(tl, op, x, y, dy, dx, steps: int, dist: Dist, flops_step: floa
                     "and written), each tile's update overlapping the GPU; host wall-clock per step"}
 
 
+def disk_bandwidth(path: str, nbytes: int, threads: int = 4, chunk: int = 16 << 20) -> tuple:
+    """Direct-I/O write then read bandwidth (GB/s) of a scratch file of
+    `nbytes` at `path`, in `chunk` requests spread over `threads` threads
+    (the file tier's own request size and thread count)."""
+    import mmap
+    import threading
+    nbytes -= nbytes % chunk
+    bufs = [mmap.mmap(-1, chunk) for _ in range(threads)]  # page-aligned, as direct I/O needs
+    for b in bufs:
+        b.write(os.urandom(4096) * (chunk // 4096))
+
+    def run(fd, write):
+        nxt = [0]
+        lock = threading.Lock()
+
+        def work(b):
+            while True:
+                with lock:
+                    off = nxt[0]
+                    nxt[0] += chunk
+                if off >= nbytes:
+                    return
+                if write:
+                    os.pwrite(fd, b, off)
+                else:
+                    os.preadv(fd, [b], off)
+        th = [threading.Thread(target=work, args=(b,)) for b in bufs]
+        t0 = time.perf_counter()
+        for t in th:
+            t.start()
+        for t in th:
+            t.join()
+        return nbytes / (time.perf_counter() - t0) / 1e9
+
+    fd = os.open(path, os.O_RDWR | os.O_CREAT | os.O_TRUNC | os.O_DIRECT, 0o644)
+    try:
+        w = run(fd, True)
+        os.fsync(fd)
+        r = run(fd, False)
+    finally:
+        os.close(fd)
+        os.unlink(path)
+    return w, r
+
+
+def run_file_tier(tl, cfg, w, x, y, dy, dx, steps: int, dist: Dist, flops_step: float, peaks: dict,
+                  tier_dir: str) -> dict:
+    """The same step with W and dW in files (tiled_linear_create_file): every
+    tile read from the W file with direct I/O into pinned host slots, every
+    dW tile written to the dW file, one storage tier below host memory."""
+    import tempfile
+
+    import torch
+    K, M, N, d = cfg["K"], cfg["M"], cfg["N"], cfg["d"]
+    work = tempfile.mkdtemp(prefix="tl_tier_", dir=tier_dir)
+    wp, dwp = os.path.join(work, "w.bin"), os.path.join(work, "dw.bin")
+    try:
+        w.tensor.view(torch.int16).numpy().tofile(wp)  # tile-major, as the tier reads it
+        bw_write, bw_read = disk_bandwidth(os.path.join(work, "probe.bin"), 2 * K * M)
+        op = tl.TiledLinearFile(K, M, N, d, wp, dwp, host_slots=4, io_threads=4)
+        s = torch.cuda.current_stream()
+        op.forward(x, y, stream=s)
+        op.backward(x, dy, dx, stream=s)
+        op.sync()
+        f0 = op.file_stats()
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            op.forward(x, y, stream=s)
+            op.backward(x, dy, dx, stream=s)
+        torch.cuda.synchronize()
+        op.sync()  # the step's dW is in its file
+        sec = dist.max((time.perf_counter() - t0) / steps)
+        f1 = op.file_stats()
+        op.close()
+    except tl.TiledLinearError as e:
+        return {"unavailable": str(e)}
+    finally:
+        for f in (wp, dwp):
+            if os.path.exists(f):
+                os.unlink(f)
+        os.rmdir(work)
+    rd = f1["read_bytes"] - f0["read_bytes"]
+    wr = f1["write_bytes"] - f0["write_bytes"]
+    R = peaks["bf16_tflops"] * 1e12
+    t_roof = max(flops_step / R, 4.0 * K * M / (bw_read * 1e9), 2.0 * K * M / (bw_write * 1e9))
+    t_serial = max(flops_step / R, 4.0 * K * M / (bw_read * 1e9) + 2.0 * K * M / (bw_write * 1e9))
+    return {"value": round(dist.world * flops_step / sec / 1e12, 2), "unit": UNIT, "ms_per_step": round(sec * 1e3, 2),
+            "steps": steps, "read_bytes_per_step": rd // steps, "write_bytes_per_step": wr // steps,
+            "disk_read_gbs": round(bw_read, 2), "disk_write_gbs": round(bw_write, 2),
+            "tier_read_gbs": round(rd / steps / sec / 1e9, 2), "tier_write_gbs": round(wr / steps / sec / 1e9, 2),
+            "fetch_wait_ms_per_step": round((f1["fetch_wait_seconds"] - f0["fetch_wait_seconds"]) / steps * 1e3, 2),
+            "step_roofline": {
+                "form": "one disk serves the reads and the writes in turn: t_roof = max(6TKM/R, 4KM/B_disk_read + "
+                        "2KM/B_disk_write); frac_if_overlapped uses max(6TKM/R, 4KM/B_read, 2KM/B_write)",
+                "roofline_tflops": round(flops_step / t_serial / 1e12, 2), "frac": round(t_serial / sec, 4),
+                "t_roof_ms": round(t_serial * 1e3, 2), "frac_if_overlapped": round(t_roof / sec, 4)},
+            "host_slots": f1["host_slots"], "io_threads": f1["io_threads"], "dir": tier_dir,
+            "what": "W and dW in files on the box's disk, read and written with direct I/O through pinned host "
+                    "slots (tiled_linear_create_file); host wall-clock per step until dW is in its file"}
+
+
 def run_ffn_chain(tl, cfg, x, y_up, dx, seed: int, steps: int, dist: Dist) -> dict:
     """The workload's layer followed by its down-projection (M -> K, N tiles of
     K/N columns, W2 [M, K] pinned, tile-major), run as one chain: one ring and
@@ -806,6 +911,10 @@ def run_ours(args, cfg, dist: Dist):
     if not args.skip_aux and not persistent and M % K == 0:
         out["ffn_chain"] = run_ffn_chain(tl, cfg, x, y, dx, args.seed, max(3, min(args.steps, 20)), dist)
 
+    # --- W and dW one tier further down: files on the box's disk -----------------
+    if not args.skip_aux and not persistent:
+        out["file_tier"] = run_file_tier(tl, cfg, w, x, y, dy, dx, 3, dist, flops_step, peaks, args.tier_dir)
+
     # --- CPU oracle baseline ----------------------------------------------------
     if want_cpu:
         xh, dyh = x.cpu(), dy.cpu()
@@ -961,6 +1070,8 @@ def main():
     ap.add_argument("--skip-aux", action="store_true",
                     help="skip the link / copy-only / resident / e2e measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tier-dir", default=os.environ.get("TMPDIR", "/tmp"),
+                    help="directory for the file tier's W and dW files (the file_tier measurement)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--sweep", action="store_true",

@@ -51,7 +51,9 @@ typedef enum {
     TL_ERR_WORKSPACE = 3,   /* workspace too small or misaligned             */
     TL_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed           */
     TL_ERR_TIMEOUT = 5,     /* a kernel's bounded wait gave up (see below)   */
-    TL_ERR_STATE = 6        /* handle already failed, or NULL                */
+    TL_ERR_STATE = 6,       /* handle already failed, or NULL                */
+    TL_ERR_IO = 7           /* a file of the file tier failed (open, read,   */
+                            /* write), see tiled_linear_create_file          */
 } tl_status;
 
 /* Host storage of W (read) and dW (written).
@@ -137,6 +139,53 @@ tl_status tiled_linear_create_tilemajor(tl_handle **out, int64_t K, int64_t M, i
                                         int32_t d, const void *w_host, void *dw_host,
                                         void *workspace_dev, size_t workspace_bytes,
                                         int device);
+
+/* File tier: W and dW live in files instead of host memory, one tier further
+ * from the GPU (ZeRO-Infinity keeps them on NVMe and moves each tile up one
+ * tier at a time: NVMe -> pinned CPU buffers with direct I/O -> GPU, the
+ * stages overlapping on different tiles; "Overlap-centric design", and the
+ * direct-I/O-into-pinned-buffers rule of memory-centric tiling, "Pitfalls").
+ *  w_path  : file holding W tile-major [N][K][Mi] bf16 (N * K*Mi*2 bytes at
+ *            least), opened read-only with O_DIRECT.
+ *  dw_path : file that receives dW in the same layout, opened with O_DIRECT
+ *            (created, and extended to N tiles if shorter).
+ *  host_slots (2..64): pinned host slots per direction, each one tile.  Reader
+ *            threads read up to host_slots tiles ahead of the host->device
+ *            copies (which run up to d tiles ahead of the GEMMs); the
+ *            device->host copies of dW land in the other host_slots slots,
+ *            which writer threads store to dw_path.
+ *  io_threads (1..64): threads per direction; each tile is read / written
+ *            as 16 MiB direct-I/O requests spread over them.
+ * A tile (K * M/N * 2 bytes) must be a multiple of 4096 bytes.  The other
+ * arguments and the workspace are as tiled_linear_create_tilemajor.  The
+ * handle runs one launch per tile (never the persistent pass) and takes no
+ * host optimizer.  A forward or backward call returns once its last copy is
+ * enqueued, so the calling thread waits for the tile reads (the GPU works on
+ * the tiles already there meanwhile), and a backward also waits for free dW
+ * slots.  dW is in dw_path only after tiled_linear_file_sync.
+ * Errors: as tiled_linear_create, and TL_ERR_IO (a file cannot be opened
+ * with direct I/O, is too short, or the pinned slots cannot be had).  A read
+ * or write that fails later makes the handle fail with TL_ERR_IO. */
+tl_status tiled_linear_create_file(tl_handle **out, int64_t K, int64_t M, int32_t N, int32_t d,
+                                   const char *w_path, const char *dw_path, int32_t host_slots,
+                                   int32_t io_threads, void *workspace_dev, size_t workspace_bytes,
+                                   int device);
+
+/* Block until every dW tile of the backward calls made so far is in dw_path.
+ * Call it after the calls' stream has been synchronised (it does not wait for
+ * work still queued on the device, only for the writers).  TL_ERR_INVALID if
+ * the handle has no file tier, TL_ERR_IO if a write failed. */
+tl_status tiled_linear_file_sync(tl_handle *h);
+
+/* Counters of the file tier since the handle was created. */
+typedef struct {
+    int64_t read_bytes, write_bytes;   /* W bytes read, dW bytes written       */
+    double read_seconds, write_seconds; /* summed wall time of the tile I/O    */
+    double fetch_wait_seconds;         /* calls waiting for a tile to be read  */
+    double writeback_wait_seconds;     /* calls waiting for a free dW slot     */
+    int32_t host_slots, io_threads;
+} tl_file_stats;
+tl_status tiled_linear_file_stats(const tl_handle *h, tl_file_stats *out);
 
 /* Forward: y_dev[T, M] (bf16, ld M) = x_dev[T, K] (bf16, ld K) . W, tile by
  * tile, fp32 accumulation, round-to-nearest-even to bf16.  T >= 0 (T = 0 is

@@ -26,7 +26,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # optimizer update gives the same bits on every host architecture
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-Xcompiler", "-ffp-contract=off", "-I", INCLUDE, "-I", CSRC]
-UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_cast.cu", "tl_adam.cpp",
+UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_cast.cu", "tl_adam.cpp", "tl_filetier.cpp",
          "tl_optimizer.cpp"]
 
 

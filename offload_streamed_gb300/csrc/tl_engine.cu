@@ -22,6 +22,7 @@
 // compute).
 #include "tiled_linear.h"
 #include "tl_cast.h"
+#include "tl_filetier.h"
 #include "tl_gemm.h"
 #include "tl_optimizer.h"
 
@@ -204,6 +205,7 @@ struct tl_handle {
     bool opt_have_bwd = false;  // a backward recorded the events since the last submit
     int num_sms = 0;
     bool persistent = false;  // whole passes as one persistent launch
+    tl::FileTier* tier = nullptr;  // W and dW in files (tiled_linear_create_file), else in host memory
     uint32_t* flags = nullptr;
     uint32_t* done = nullptr;
     uint32_t* dwdone = nullptr;
@@ -233,7 +235,7 @@ struct DeviceGuard {
 tl_status fail(tl_handle* h, tl_status st, const std::string& what) {
     if (h) {
         h->msg = what;
-        if (st == TL_ERR_CUDA || st == TL_ERR_TIMEOUT) h->sticky = st;
+        if (st == TL_ERR_CUDA || st == TL_ERR_TIMEOUT || st == TL_ERR_IO) h->sticky = st;
     }
     return st;
 }
@@ -338,6 +340,41 @@ cudaError_t copy_dw_tile(const Op& o, int i, const void* src, cudaStream_t st) {
         return cudaMemcpyAsync(dw_tile_dst(o, i), src, tile_bytes(s.K, s.Mi), cudaMemcpyDeviceToHost, st);
     return cudaMemcpy2DAsync(dw_tile_dst(o, i), size_t(s.M) * 2, src, size_t(s.Mi) * 2,
                              size_t(s.Mi) * 2, size_t(s.K), cudaMemcpyDeviceToHost, st);
+}
+
+// Host->device copy of W tile i of operator o into device slot dst on the
+// h2d stream: from pinned host memory, or from the file tier's host slot
+// once its reader has the tile there (the calling thread waits for that).
+tl_status fetch_w_tile(tl_handle* h, const Op& o, int i, void* dst) {
+    if (!h->tier) {
+        TL_TRY(h, copy_w_tile(o, i, dst, h->h2d));
+        return TL_OK;
+    }
+    std::string why;
+    const int slot = h->tier->acquire_w(o.first + i, &why);
+    if (slot < 0) return fail(h, TL_ERR_IO, why);
+    TL_TRY(h, cudaMemcpyAsync(dst, h->tier->w_slot(slot), tile_bytes(o.s.K, o.s.Mi), cudaMemcpyHostToDevice, h->h2d));
+    TL_TRY(h, cudaEventRecord(h->tier->w_event(slot), h->h2d));
+    h->tier->release_w(slot);
+    return TL_OK;
+}
+
+// Device->host copy of dW tile i of operator o from src on stream st: into
+// pinned host memory, or into a file-tier host slot that a writer stores
+// to the dW file once the copy is done (the calling thread waits for a free
+// slot).
+tl_status writeback_dw_tile(tl_handle* h, const Op& o, int i, const void* src, cudaStream_t st) {
+    if (!h->tier) {
+        TL_TRY(h, copy_dw_tile(o, i, src, st));
+        return TL_OK;
+    }
+    std::string why;
+    const int slot = h->tier->acquire_dw(&why);
+    if (slot < 0) return fail(h, TL_ERR_IO, why);
+    TL_TRY(h, cudaMemcpyAsync(h->tier->dw_slot(slot), src, tile_bytes(o.s.K, o.s.Mi), cudaMemcpyDeviceToHost, st));
+    TL_TRY(h, cudaEventRecord(h->tier->dw_event(slot), st));
+    h->tier->commit_dw(slot, o.first + i);
+    return TL_OK;
 }
 
 float span_ms(cudaEvent_t a, cudaEvent_t b) {
@@ -539,7 +576,8 @@ tl_status enqueue_fetches(tl_handle* h, CallSlot& t, uint64_t base, bool backwar
         if (f >= nslots)
             TL_CU(h, mo.wait(cu(h->h2d), cuptr(h->flags + tl::kFlagFreed + sl), uint32_t(f - nslots + 1), kWaitGeq));
         TL_TRY(h, cudaEventRecord(t.ev[4][j], h->h2d));
-        TL_TRY(h, copy_w_tile(h->ops[0], i, h->slot[sl], h->h2d));
+        const tl_status st = fetch_w_tile(h, h->ops[0], i, h->slot[sl]);
+        if (st != TL_OK) return st;
         TL_TRY(h, cudaEventRecord(t.ev[5][j], h->h2d));
         TL_CU(h, mo.write(cu(h->h2d), cuptr(h->flags + tl::kFlagReady + sl), uint32_t(f + 1), kWriteDefault));
     }
@@ -562,8 +600,15 @@ tl_status launch(tl_handle* h, const tl::GemmDesc& g0, cudaStream_t st) {
 }
 
 // Create a handle over `ops` (one operator, or a chain) sharing one ring.
+// W and dW in files instead of host memory (tiled_linear_create_file).
+struct FileArgs {
+    const char* w_path = nullptr;
+    const char* dw_path = nullptr;
+    int32_t host_slots = 0, io_threads = 0;
+};
+
 tl_status create_ops(tl_handle** out, std::vector<Op> ops, int32_t d, void* ws, size_t ws_bytes, int device,
-                     bool single_api) {
+                     bool single_api, const FileArgs* file = nullptr) {
     if (!out) {
         g_create_error = "out is NULL";
         return TL_ERR_INVALID;
@@ -575,7 +620,7 @@ tl_status create_ops(tl_handle** out, std::vector<Op> ops, int32_t d, void* ws, 
     for (size_t l = 0; l < ops.size() && bad.empty(); ++l) {
         Op& o = ops[l];
         bad = check_shape(o.s.K, o.s.M, o.s.N, d);
-        if (bad.empty() && (!o.w_host || !o.dw_host)) bad = "null pointer argument";
+        if (bad.empty() && !file && (!o.w_host || !o.dw_host)) bad = "null pointer argument";
         if (bad.empty() && l > 0 && o.s.K != ops[l - 1].s.M) bad = "operator inputs must match the outputs before them";
         if (!bad.empty() && ops.size() > 1) bad = "operator " + std::to_string(l) + ": " + bad;
         o.s.Mi = o.s.M / std::max<int32_t>(o.s.N, 1);
@@ -626,7 +671,7 @@ tl_status create_ops(tl_handle** out, std::vector<Op> ops, int32_t d, void* ws, 
         return bail(TL_ERR_CUDA);
     }
     for (const Op& o : ops)
-        if (!is_pinned_host(o.w_host) || !is_pinned_host(o.dw_host)) {
+        if (!file && (!is_pinned_host(o.w_host) || !is_pinned_host(o.dw_host))) {
             h->msg = "w_host and dw_host must be pinned host memory";
             return bail(TL_ERR_NOT_PINNED);
         }
@@ -705,12 +750,21 @@ tl_status create_ops(tl_handle** out, std::vector<Op> ops, int32_t d, void* ws, 
         probe.x = h->ws;
         probe.y = h->ws;
         const MemOps& mo = memops();
-        if (wanted && single_api && mo.write && mo.wait && tl::pass_check(probe, h->num_sms).empty()) {
+        if (wanted && single_api && !file && mo.write && mo.wait && tl::pass_check(probe, h->num_sms).empty()) {
             // the stream memory operations must work on this device
             if (mo.write(cu(h->h2d), cuptr(h->flags + tl::kNumFlags), 0u, kWriteDefault) == CUDA_SUCCESS &&
                 cudaStreamSynchronize(h->h2d) == cudaSuccess && tl::pass_preload() == cudaSuccess)
                 h->persistent = true;
             cudaGetLastError();
+        }
+    }
+    if (file) {
+        std::string why;
+        h->tier = tl::FileTier::open(file->w_path, file->dw_path, N, tile_bytes(h->s.K, h->s.Mi), file->host_slots,
+                                     file->io_threads, &why);
+        if (!h->tier) {
+            h->msg = "file tier: " + why;
+            return bail(TL_ERR_IO);
         }
     }
     *out = h;
@@ -765,7 +819,8 @@ tl_status backward_persistent(tl_handle* h, int64_t T, const void* x, const void
         TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_call_done, 0));
         TL_TRY(h, cudaStreamWaitEvent(cs, h->ev_d2h_tail, 0));
         TL_TRY(h, cudaMemsetAsync(h->stage[0], 0, tb, cs));
-        for (int i = 0; i < s.N; ++i) TL_TRY(h, copy_dw_tile(h->ops[0], i, h->stage[0], cs));
+        for (int i = 0; i < s.N; ++i)
+            if ((st = writeback_dw_tile(h, h->ops[0], i, h->stage[0], cs)) != TL_OK) return st;
         TL_TRY(h, cudaEventRecord(h->ev_call_done, cs));
         return TL_OK;
     }
@@ -794,7 +849,7 @@ tl_status backward_persistent(tl_handle* h, int64_t T, const void* x, const void
         const int g = int(sj % uint64_t(h->nstage));
         TL_CU(h, mo.wait(cu(h->d2h), cuptr(h->flags + tl::kFlagDwReady + g), uint32_t(sj + 1), kWaitGeq));
         TL_TRY(h, cudaEventRecord(t.ev[6][j], h->d2h));
-        TL_TRY(h, copy_dw_tile(h->ops[0], i, h->stage[g], h->d2h));
+        if ((st = writeback_dw_tile(h, h->ops[0], i, h->stage[g], h->d2h)) != TL_OK) return st;
         TL_TRY(h, cudaEventRecord(t.ev[7][j], h->d2h));
         TL_CU(h, mo.write(cu(h->d2h), cuptr(h->flags + tl::kFlagDrained + g), uint32_t(sj + 1), kWriteDefault));
     }
@@ -822,6 +877,10 @@ tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys,
     if (!tp) return st;
     CallSlot& t = *tp;
     int64_t h2d_bytes = 0;
+    if (h->tier) {  // the file tier reads the tiles in the order this call fetches them
+        h->tier->clear_requests();
+        for (int g = 0; g < h->n_total; ++g) h->tier->request(g);
+    }
     TL_TRY(h, cudaEventRecord(t.start, cs));
     for (size_t l = 0; l < h->ops.size(); ++l) {
         const Op& o = h->ops[l];
@@ -837,7 +896,7 @@ tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys,
             h->slot_tile[size_t(sl)] = -1;
             TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
             if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[4][g], h->h2d));
-            TL_TRY(h, copy_w_tile(o, i, h->slot[sl], h->h2d));
+            if ((st = fetch_w_tile(h, o, i, h->slot[sl])) != TL_OK) return st;
             h->slot_tile[size_t(sl)] = g;
             h2d_bytes += int64_t(tile_bytes(s.K, s.Mi));
             if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[5][g], h->h2d));
@@ -896,7 +955,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             for (int i = o.s.N - 1; i >= 0; --i) {
                 const int g = o.first + i;
                 if ((st = opt_wait(h, g, false)) != TL_OK) return st;
-                TL_TRY(h, copy_dw_tile(o, i, h->stage[0], cs));
+                if ((st = writeback_dw_tile(h, o, i, h->stage[0], cs)) != TL_OK) return st;
                 if (h->opt) {
                     TL_TRY(h, cudaEventRecord(h->opt_ev_w[size_t(g)], cs));
                     TL_TRY(h, cudaEventRecord(h->opt_ev_dw[size_t(g)], cs));
@@ -934,6 +993,13 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
         h->slot_q.swap(q);
     }
     int64_t h2d_bytes = 0, d2h_bytes = 0;
+    if (h->tier) {  // the tiles this call fetches, in its order (operators and tiles descending)
+        h->tier->clear_requests();
+        int pos = 0;
+        for (int l = L - 1; l >= 0; --l)
+            for (int i = h->ops[size_t(l)].s.N - 1; i >= 0; --i, ++pos)
+                if (pos >= reused) h->tier->request(h->ops[size_t(l)].first + i);
+    }
     int launches = 0;
     int jg = 0;  // position in the backward's tile order
     std::vector<bool> stage_ready(size_t(h->nstage), false);  // forward done with the staging slot
@@ -967,7 +1033,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
                 h->slot_tile[size_t(sl)] = -1;
                 TL_TRY(h, cudaStreamWaitEvent(h->h2d, h->ev_free[sl], 0));
                 if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[4][jg], h->h2d));
-                TL_TRY(h, copy_w_tile(o, i, h->slot[sl], h->h2d));
+                if ((st = fetch_w_tile(h, o, i, h->slot[sl])) != TL_OK) return st;
                 if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[5][jg], h->h2d));
                 TL_TRY(h, cudaEventRecord(h->ev_ready[sl], h->h2d));
                 h->slot_tile[size_t(sl)] = g;
@@ -1007,7 +1073,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             if ((st = opt_wait(h, g, false)) != TL_OK) return st;
             TL_TRY(h, cudaStreamWaitEvent(h->d2h, h->ev_dwdone[gs], 0));
             if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[6][jg], h->d2h));
-            TL_TRY(h, copy_dw_tile(o, i, h->stage[gs], h->d2h));
+            if ((st = writeback_dw_tile(h, o, i, h->stage[gs], h->d2h)) != TL_OK) return st;
             if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[7][jg], h->d2h));
             if (h->opt) {
                 TL_TRY(h, cudaEventRecord(h->opt_ev_dw[size_t(g)], h->d2h));
@@ -1119,6 +1185,53 @@ tl_status tiled_linear_create_tilemajor(tl_handle** out, int64_t K, int64_t M, i
                                         size_t workspace_bytes, int device) {
     return create_ops(out, {one_op(K, M, N, w_host, dw_host, TL_LAYOUT_TILE_MAJOR)}, d, workspace_dev,
                       workspace_bytes, device, true);
+}
+
+tl_status tiled_linear_create_file(tl_handle** out, int64_t K, int64_t M, int32_t N, int32_t d, const char* w_path,
+                                   const char* dw_path, int32_t host_slots, int32_t io_threads, void* workspace_dev,
+                                   size_t workspace_bytes, int device) {
+    std::string bad;
+    if (!w_path || !dw_path || !w_path[0] || !dw_path[0]) bad = "null or empty file path";
+    else if (host_slots < 2 || host_slots > 64) bad = "host_slots must be in 2..64";
+    else if (io_threads < 1 || io_threads > 64) bad = "io_threads must be in 1..64";
+    else if (check_shape(K, M, N, d).empty() && (K * (M / N) * 2) % 4096)
+        bad = "a tile (K * M/N * 2 bytes) must be a multiple of 4096 bytes for direct I/O";
+    if (!bad.empty()) {
+        g_create_error = bad;
+        if (out) *out = nullptr;
+        return TL_ERR_INVALID;
+    }
+    FileArgs fa;
+    fa.w_path = w_path;
+    fa.dw_path = dw_path;
+    fa.host_slots = host_slots;
+    fa.io_threads = io_threads;
+    return create_ops(out, {one_op(K, M, N, nullptr, nullptr, TL_LAYOUT_TILE_MAJOR)}, d, workspace_dev,
+                      workspace_bytes, device, true, &fa);
+}
+
+tl_status tiled_linear_file_sync(tl_handle* h) {
+    if (!h) return TL_ERR_STATE;
+    if (!h->tier) return fail(h, TL_ERR_INVALID, "the handle keeps W and dW in host memory");
+    std::string why;
+    if (!h->tier->sync(&why)) return fail(h, TL_ERR_IO, "file tier: " + why);
+    return TL_OK;
+}
+
+tl_status tiled_linear_file_stats(const tl_handle* h, tl_file_stats* out) {
+    if (!h || !out) return TL_ERR_INVALID;
+    if (!h->tier) return TL_ERR_INVALID;
+    const tl::FileTierStats st = h->tier->stats();
+    std::memset(out, 0, sizeof(*out));
+    out->read_bytes = st.read_bytes;
+    out->write_bytes = st.write_bytes;
+    out->read_seconds = st.read_s;
+    out->write_seconds = st.write_s;
+    out->fetch_wait_seconds = st.fetch_wait_s;
+    out->writeback_wait_seconds = st.writeback_wait_s;
+    out->host_slots = h->tier->host_slots();
+    out->io_threads = h->tier->io_threads();
+    return TL_OK;
 }
 
 static std::string chain_args(int32_t L, const int64_t* dims, const int32_t* n_tiles) {
@@ -1285,6 +1398,8 @@ tl_status tiled_linear_destroy(tl_handle* h) {
         detach_optimizer(h);
         if (h->h2d) cudaStreamSynchronize(h->h2d);
         if (h->d2h) cudaStreamSynchronize(h->d2h);
+        delete h->tier;  // stores the dW tiles still being written
+        h->tier = nullptr;
         for (auto* v : {&h->ev_ready, &h->ev_free, &h->ev_dwdone, &h->ev_drained})
             for (auto e : *v) {
                 if (e) {
@@ -1421,6 +1536,7 @@ tl_status tiled_linear_optimizer_create(tl_optimizer** out, tl_handle* h, const 
     const std::string bad = adam_config_error(cfg);
     if (!bad.empty()) return fail(h, TL_ERR_INVALID, "optimizer config: " + bad);
     if (h->persistent) return fail(h, TL_ERR_INVALID, "the host optimizer needs the per-tile launch mode");
+    if (h->tier) return fail(h, TL_ERR_INVALID, "the host optimizer needs W and dW in host memory");
     if (h->opt) return fail(h, TL_ERR_STATE, "the handle already has an optimizer");
     if (!master || !m || !v) return fail(h, TL_ERR_INVALID, "null master, m or v array");
     std::vector<tl::Block> tiles;

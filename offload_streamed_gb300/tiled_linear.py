@@ -16,9 +16,10 @@ import threading
 
 from . import _build
 
-TL_OK, TL_ERR_INVALID, TL_ERR_NOT_PINNED, TL_ERR_WORKSPACE, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_STATE = range(7)
+(TL_OK, TL_ERR_INVALID, TL_ERR_NOT_PINNED, TL_ERR_WORKSPACE, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_STATE,
+ TL_ERR_IO) = range(8)
 STATUS_NAMES = {0: "TL_OK", 1: "TL_ERR_INVALID", 2: "TL_ERR_NOT_PINNED", 3: "TL_ERR_WORKSPACE",
-                4: "TL_ERR_CUDA", 5: "TL_ERR_TIMEOUT", 6: "TL_ERR_STATE"}
+                4: "TL_ERR_CUDA", 5: "TL_ERR_TIMEOUT", 6: "TL_ERR_STATE", 7: "TL_ERR_IO"}
 
 
 class TiledLinearError(RuntimeError):
@@ -47,6 +48,16 @@ class tl_stats(ctypes.Structure):
         ("bwd_reused_tiles", ctypes.c_int32),
         ("fwd_timed_calls", ctypes.c_int64), ("bwd_timed_calls", ctypes.c_int64), ("timing_every", ctypes.c_int32),
     ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class tl_file_stats(ctypes.Structure):
+    _fields_ = [("read_bytes", ctypes.c_int64), ("write_bytes", ctypes.c_int64),
+                ("read_seconds", ctypes.c_double), ("write_seconds", ctypes.c_double),
+                ("fetch_wait_seconds", ctypes.c_double), ("writeback_wait_seconds", ctypes.c_double),
+                ("host_slots", ctypes.c_int32), ("io_threads", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -84,6 +95,13 @@ def load():
             fn = getattr(L, name)
             fn.argtypes = [ctypes.POINTER(vp), i64, i64, i32, i32, vp, vp, vp, sz, ctypes.c_int]
             fn.restype = st
+        L.tiled_linear_create_file.argtypes = [ctypes.POINTER(vp), i64, i64, i32, i32, ctypes.c_char_p,
+                                               ctypes.c_char_p, i32, i32, vp, sz, ctypes.c_int]
+        L.tiled_linear_create_file.restype = st
+        L.tiled_linear_file_sync.argtypes = [vp]
+        L.tiled_linear_file_sync.restype = st
+        L.tiled_linear_file_stats.argtypes = [vp, vp]
+        L.tiled_linear_file_stats.restype = st
         L.tiled_linear_forward.argtypes = [vp, i64, vp, vp, vp]
         L.tiled_linear_forward.restype = st
         L.tiled_linear_backward.argtypes = [vp, i64, vp, vp, vp, vp]
@@ -165,6 +183,26 @@ def tiled_linear_create_tilemajor(K, M, N, d, w_host, dw_host, workspace_dev, wo
                                   device) -> int:
     return tiled_linear_create(K, M, N, d, w_host, dw_host, workspace_dev, workspace_bytes, device,
                                tile_major=True)
+
+
+def tiled_linear_create_file(K, M, N, d, w_path: str, dw_path: str, host_slots: int, io_threads: int,
+                             workspace_dev, workspace_bytes, device) -> int:
+    """W and dW in files (tile-major), streamed through pinned host slots."""
+    h = ctypes.c_void_p()
+    _check(load().tiled_linear_create_file(ctypes.byref(h), K, M, N, d, os.fsencode(w_path), os.fsencode(dw_path),
+                                           host_slots, io_threads, workspace_dev, workspace_bytes, device),
+           "tiled_linear_create_file")
+    return h.value
+
+
+def tiled_linear_file_sync(h: int) -> None:
+    _check(load().tiled_linear_file_sync(h), "tiled_linear_file_sync", h)
+
+
+def tiled_linear_file_stats(h: int) -> dict:
+    s = tl_file_stats()
+    _check(load().tiled_linear_file_stats(h, ctypes.byref(s)), "tiled_linear_file_stats", h)
+    return s.as_dict()
 
 
 def tiled_linear_forward(h: int, T: int, x_dev: int, y_dev: int, stream: int) -> None:
@@ -437,6 +475,42 @@ class TiledLinear:
             pass
 
 
+class TiledLinearFile(TiledLinear):
+    """A ``TiledLinear`` whose W and dW live in files (tile-major [N][K][M/N]
+    bf16), one storage tier below host memory: reader threads stream the
+    tiles into pinned host slots with direct I/O, ahead of the host->device
+    copies, and writer threads store dW.  ``sync()`` waits until the dW of the
+    backward calls made so far is in ``dw_path``."""
+
+    def __init__(self, K: int, M: int, N: int, d: int, w_path: str, dw_path: str, *, host_slots: int = 4,
+                 io_threads: int = 4, device=None):
+        import torch
+        self.K, self.M, self.N, self.d = int(K), int(M), int(N), int(d)
+        self.Mi = self.M // self.N
+        self.tile_major = True
+        self.w_path, self.dw_path = str(w_path), str(dw_path)
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
+                                   torch.device(device).index or 0)
+        self.handle = 0
+        wb = tiled_linear_workspace_bytes(self.K, self.M, self.N, self.d)
+        if wb == 0:
+            raise TiledLinearError(TL_ERR_INVALID, "tiled_linear_workspace_bytes",
+                                   f"invalid shape K={K} M={M} N={N} d={d}")
+        self.workspace = torch.empty(wb, dtype=torch.uint8, device=self.device)
+        self.handle = tiled_linear_create_file(self.K, self.M, self.N, self.d, self.w_path, self.dw_path,
+                                               int(host_slots), int(io_threads), self.workspace.data_ptr(), wb,
+                                               self.device.index)
+
+    def sync(self) -> None:
+        """Wait for the device, then for the writers: dW is in ``dw_path``."""
+        import torch
+        torch.cuda.synchronize(self.device)
+        tiled_linear_file_sync(self.handle)
+
+    def file_stats(self) -> dict:
+        return tiled_linear_file_stats(self.handle)
+
+
 class TiledLinearChain:
     """A chain of tiled linear operators (see the chain section of
     ``include/tiled_linear.h``): operator l maps dims[l] -> dims[l+1] with its
@@ -525,6 +599,9 @@ class HostAdam:
                  accumulate=False):
         import torch
         self.op = op
+        self.handle = 0
+        if getattr(op, "_w", None) is None:
+            raise TiledLinearError(TL_ERR_INVALID, "HostAdam", "the host optimizer needs W and dW in host memory")
         ws = op._w if isinstance(op._w, list) else [op._w]
         hosts = [b.tensor if isinstance(b, PinnedBuffer) else b for b in ws]
         self.master = [h.view(-1).float() for h in hosts]

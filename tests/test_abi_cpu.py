@@ -115,24 +115,50 @@ def test_null_handle_tile_reuse(tl):
     assert tl.load().tiled_linear_set_tile_reuse(None, 1) == tl.TL_ERR_STATE
 
 
-def test_stats_struct_layout_matches_the_header(tl, tmp_path):
-    """The binding's tl_stats mirrors the C struct field by field: a C program
+@pytest.mark.parametrize("struct", ["tl_stats", "tl_file_stats", "tl_adam_config"])
+def test_stats_struct_layout_matches_the_header(tl, tmp_path, struct):
+    """The binding's structs mirror the C structs field by field: a C program
     built against include/tiled_linear.h prints sizeof and every offsetof."""
     import shutil
     import subprocess
     if shutil.which("gcc") is None:
         pytest.skip("gcc missing")
-    fields = [name for name, _ in tl.tl_stats._fields_]
+    cls = getattr(tl, struct)
+    fields = [name for name, _ in cls._fields_]
     src = tmp_path / "layout.c"
     src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"tiled_linear.h\"\nint main(void) {\n"
-                   "  printf(\"%zu\\n\", sizeof(tl_stats));\n"
-                   + "".join(f"  printf(\"%zu\\n\", offsetof(tl_stats, {f}));\n" for f in fields)
+                   f"  printf(\"%zu\\n\", sizeof({struct}));\n"
+                   + "".join(f"  printf(\"%zu\\n\", offsetof({struct}, {f}));\n" for f in fields)
                    + "  return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
-    assert out[0] == ctypes.sizeof(tl.tl_stats)
-    assert out[1:] == [getattr(tl.tl_stats, f).offset for f in fields]
+    assert out[0] == ctypes.sizeof(cls)
+    assert out[1:] == [getattr(cls, f).offset for f in fields]
+
+
+def test_file_tier_argument_checks(tl, tmp_path):
+    """Paths, slot and thread counts and the direct-I/O tile size are refused
+    before any CUDA call or file access."""
+    lib = tl.load()
+    w, dw = str(tmp_path / "w.bin").encode(), str(tmp_path / "dw.bin").encode()
+    h = ctypes.c_void_p()
+    K, M, N = 256, 1024, 4  # tile = 256 * 256 * 2 bytes, a multiple of 4096
+    args = lambda **kw: dict(dict(w=w, dw=dw, slots=4, io=2, K=K, M=M, N=N), **kw)
+    def create(a):
+        return lib.tiled_linear_create_file(ctypes.byref(h), a["K"], a["M"], a["N"], 1, a["w"], a["dw"],
+                                            a["slots"], a["io"], 256, 1 << 30, 0)
+    assert create(args(w=None)) == tl.TL_ERR_INVALID
+    assert create(args(dw=b"")) == tl.TL_ERR_INVALID
+    assert create(args(slots=1)) == tl.TL_ERR_INVALID
+    assert create(args(slots=65)) == tl.TL_ERR_INVALID
+    assert create(args(io=0)) == tl.TL_ERR_INVALID
+    assert create(args(K=8, M=64, N=8)) == tl.TL_ERR_INVALID  # 128-byte tiles: no direct I/O
+    assert create(args(K=256, M=1000, N=4)) == tl.TL_ERR_INVALID  # tile width 250: not a multiple of 8
+    assert h.value is None
+    assert lib.tiled_linear_file_sync(None) == tl.TL_ERR_STATE
+    assert lib.tiled_linear_file_stats(None, None) == tl.TL_ERR_INVALID
+    assert not (tmp_path / "dw.bin").exists()  # nothing was opened
 
 
 def test_chain_workspace_and_scratch_bytes(tl):
