@@ -99,3 +99,39 @@ def test_random_chains(tl, seed):
     assert ch.close() == tl.TL_OK
     for b in w + dw:
         b.close()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_file_tier(tl, tmp_path, seed):
+    """Random shapes, depths, host slots, I/O threads, reuse and call counts
+    through the file tier: bit-identical to the host-memory path (which the
+    cases above check against the oracle)."""
+    rng = np.random.default_rng(3000 + seed)
+    N = int(rng.integers(1, 7))
+    Mi = 8 * int(rng.integers(1, 49))
+    K = 256 * int(rng.integers(1, 4))          # K * Mi * 2 bytes: a multiple of 4096 for direct I/O
+    M, T = N * Mi, int(rng.integers(1, 300))
+    d = int(rng.integers(-1, N + 2))
+    slots, io = int(rng.integers(2, 6)), int(rng.integers(1, 5))
+    reuse, calls = bool(rng.integers(0, 2)), int(rng.integers(1, 4))
+    w, dw = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
+    I.fill_w_host(w.tensor, K, M, N, True, seed)
+    w.tensor.view(torch.int16).numpy().tofile(tmp_path / "w.bin")
+    x, dy = I.make_x(T, K, seed).cuda(), I.make_dy(T, M, seed).cuda()
+    ops = [tl.TiledLinear(K, M, N, d, w, dw, tile_major=True),
+           tl.TiledLinearFile(K, M, N, d, tmp_path / "w.bin", tmp_path / "dw.bin", host_slots=slots, io_threads=io)]
+    outs = []
+    for op in ops:
+        op.set_tile_reuse(reuse)
+        for _ in range(calls):
+            y = op.forward(x)
+            dx = op.backward(x, dy)
+        torch.cuda.synchronize()
+        outs.append((y.cpu().view(torch.int16), dx.cpu().view(torch.int32)))
+    ops[1].sync()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1]), (T, K, M, N, d, slots, io)
+    assert np.array_equal(np.fromfile(tmp_path / "dw.bin", dtype=np.int16), dw.tensor.view(torch.int16).numpy())
+    for op in ops:
+        assert op.close() == tl.TL_OK
+    w.close()
+    dw.close()
