@@ -26,6 +26,9 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # optimizer update gives the same bits on every host architecture
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-Xcompiler", "-ffp-contract=off", "-I", INCLUDE, "-I", CSRC]
+# Extra flags of single units: the host optimizer's row loop vectorizes its
+# square roots only without errno semantics.
+UNIT_FLAGS = {"tl_adam.cpp": ["-Xcompiler", "-fno-math-errno"]}
 UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_cast.cu", "tl_adam.cpp", "tl_filetier.cpp",
          "tl_optimizer.cpp"]
 
@@ -60,7 +63,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs, procs = [], []
     for u in UNITS:
         obj = os.path.join(LIBDIR, f"{os.path.splitext(u)[0]}.{os.getpid()}.o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, u), "-o", obj]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *UNIT_FLAGS.get(u, []), "-c", os.path.join(CSRC, u), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((u, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

@@ -47,6 +47,38 @@ void accumulate_rows(const Block& b, bool overwrite, int64_t r0, int64_t r1) {
     }
 }
 
+// f32_to_bf16 without branches, so that a row's loop vectorizes: the same
+// bits for every input (NaN keeps its payload's top and is made quiet).
+static inline uint16_t f32_to_bf16_row(float x) {
+    uint32_t u;
+    std::memcpy(&u, &x, sizeof u);
+    const uint32_t rounded = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+    const bool nan = (u & 0x7FFFFFFFu) > 0x7F800000u;
+    return uint16_t(nan ? ((u >> 16) | 0x0040u) : rounded);
+}
+
+// One row of the update: every element takes the same operations in the same
+// order, with no branch, so the compiler vectorizes the row (sqrt included:
+// this unit is built with -fno-math-errno; v is a sum of squares, never
+// negative, so sqrt would never have set errno anyway).
+template <bool ACC>
+static void adam_row(float* __restrict p, float* __restrict m, float* __restrict v, const uint16_t* __restrict g16,
+                     const float* __restrict acc, uint16_t* __restrict w, int64_t n, float b1, float c1, float b2,
+                     float c2, float step_size, float inv_sqrt_bc2, float eps, float decay) {
+    for (int64_t c = 0; c < n; ++c) {
+        float g = bf16_to_f32(g16[c]);
+        if (ACC) g = acc[c] + g;
+        const float mn = b1 * m[c] + c1 * g;
+        const float vn = b2 * v[c] + c2 * (g * g);
+        const float denom = std::sqrt(vn) * inv_sqrt_bc2 + eps;
+        const float pn = p[c] - step_size * (mn / denom) - decay * p[c];
+        m[c] = mn;
+        v[c] = vn;
+        p[c] = pn;
+        w[c] = f32_to_bf16_row(pn);
+    }
+}
+
 void adam_rows(const Block& b, const AdamHyper& hp, int64_t step, bool use_acc, int64_t r0, int64_t r1) {
     // bias corrections in double, once per call
     const double bc1 = 1.0 - std::pow(double(hp.beta1), double(step));
@@ -57,23 +89,12 @@ void adam_rows(const Block& b, const AdamHyper& hp, int64_t step, bool use_acc, 
     const float eps = hp.eps, decay = hp.lr * hp.weight_decay;
     for (int64_t r = r0; r < r1; ++r) {
         const int64_t o = r * b.ld;
-        float* p = b.master + o;
-        float* m = b.m + o;
-        float* v = b.v + o;
-        const uint16_t* g16 = b.grad + o;
-        const float* acc = use_acc ? b.acc + o : nullptr;
-        uint16_t* w = b.w + o;
-        for (int64_t c = 0; c < b.cols; ++c) {
-            const float g = acc ? acc[c] + bf16_to_f32(g16[c]) : bf16_to_f32(g16[c]);
-            const float mn = b1 * m[c] + c1 * g;
-            const float vn = b2 * v[c] + c2 * (g * g);
-            const float denom = std::sqrt(vn) * inv_sqrt_bc2 + eps;
-            const float pn = p[c] - step_size * (mn / denom) - decay * p[c];
-            m[c] = mn;
-            v[c] = vn;
-            p[c] = pn;
-            w[c] = f32_to_bf16(pn);
-        }
+        if (use_acc)
+            adam_row<true>(b.master + o, b.m + o, b.v + o, b.grad + o, b.acc + o, b.w + o, b.cols, b1, c1, b2, c2,
+                           step_size, inv_sqrt_bc2, eps, decay);
+        else
+            adam_row<false>(b.master + o, b.m + o, b.v + o, b.grad + o, nullptr, b.w + o, b.cols, b1, c1, b2, c2,
+                            step_size, inv_sqrt_bc2, eps, decay);
     }
 }
 
