@@ -872,6 +872,8 @@ def run_ours(args, cfg, dist: Dist):
         e_ms = dist.max(e_ms)
         out["e2e"] = {"value": round(dist.world * flops_step / (e_ms / 1e3) / 1e12, 2), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4),
+                      # the weight tiles the step streams besides (W in twice, dW out once)
+                      "weight_h2d_bytes_per_step": 4 * K * M, "weight_d2h_bytes_per_step": 2 * K * M,
                       "what": "X, dY copied from pinned host memory and Y, dX read back every step "
                               "(weights streamed as always), activations double-buffered across steps"}
 
