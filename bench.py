@@ -535,6 +535,47 @@ def run_host_adam(tl, op, x, y, dy, dx, steps: int, dist: Dist, flops_step: floa
                     "and written), each tile's update overlapping the GPU; host wall-clock per step"}
 
 
+def oracle_extras(xh, dyh, w_rowmajor_bits, rate_tflops: float, seed: int) -> dict:
+    """Further timings of the oracle as it stands, on the host cores:
+    (i) the tiny configuration in full (fwd + bwd) on one core and on all;
+    (ii) the sampled check of this workload (4096 seeded entries of each of Y,
+    dX and dW, plus the tile-edge entries), as the full-size parity tests run
+    it; (iii) the full problem's time extrapolated from the measured rate,
+    which is an estimate, not a measurement."""
+    import numpy as np
+
+    from oracle import oracle as O
+    from offload_streamed_gb300 import inputs as I
+    out = {}
+    tiny = CONFIGS["tiny"]
+    Tt, Kt, Mt = tiny["T"], tiny["K"], tiny["M"]
+    X = I.bits(I.make_x(Tt, Kt, seed))
+    dY = I.bits(I.make_dy(Tt, Mt, seed))
+    W = I.bits(I.make_w_tile(Kt, Mt, 0, seed))
+    cores = O.max_threads()
+    for label, n in (("one_core_s", 1), ("all_cores_s", cores)):
+        O.set_threads(n)
+        t0 = time.perf_counter()
+        O.forward(X, W)
+        O.backward(X, W, dY)
+        out[label] = round(time.perf_counter() - t0, 4)
+    O.set_threads(cores)
+    out = {"tiny_full_fwd_bwd": dict(out, flops=6.0 * Tt * Kt * Mt, cores=cores)}
+    T, K = xh.shape
+    M = w_rowmajor_bits.shape[1]
+    xb, dyb = I.bits(xh), I.bits(dyh)
+    t0 = time.perf_counter()
+    for tid, (nr, nc, fn, a, b) in enumerate([(T, M, O.sample_y, xb, w_rowmajor_bits),
+                                               (T, K, O.sample_dx, dyb, w_rowmajor_bits),
+                                               (K, M, O.sample_dw, xb, dyb)]):
+        r, c = I.sample_indices(nr, nc, 4096, seed, tid)
+        fn(a, b, r, c)
+    out["sampled_check_s"] = round(time.perf_counter() - t0, 3)
+    out["full_problem_s_est"] = round(6.0 * T * K * M / (rate_tflops * 1e12), 1)
+    out["full_problem_note"] = "estimate: 6TKM at the measured sample rate, not run"
+    return out
+
+
 def disk_bandwidth(path: str, nbytes: int, threads: int = 4, chunk: int = 16 << 20) -> tuple:
     """Direct-I/O write then read bandwidth (GB/s) of a scratch file of
     `nbytes` at `path`, in `chunk` requests spread over `threads` threads
@@ -921,6 +962,7 @@ def run_ours(args, cfg, dist: Dist):
     if want_cpu:
         xh, dyh = x.cpu(), dy.cpu()
         out["cpu_baseline"] = oracle_baseline(xh, dyh, w_rm, target_s=args.cpu_seconds)
+        out["cpu_baseline"].update(oracle_extras(xh, dyh, w_rm, out["cpu_baseline"]["value"], args.seed))
 
     op.close()
     w.close()
