@@ -576,6 +576,50 @@ def oracle_extras(xh, dyh, w_rowmajor_bits, rate_tflops: float, seed: int) -> di
     return out
 
 
+def _union(iv):
+    """Merged [start, end) intervals."""
+    out = []
+    for a, b in sorted(iv):
+        if out and a <= out[-1][1]:
+            out[-1][1] = max(out[-1][1], b)
+        else:
+            out.append([a, b])
+    return out
+
+
+def _overlap(x, y):
+    i = j = 0
+    tot = 0.0
+    while i < len(x) and j < len(y):
+        a, b = max(x[i][0], y[j][0]), min(x[i][1], y[j][1])
+        tot += max(0.0, b - a)
+        if x[i][1] < y[j][1]:
+            i += 1
+        else:
+            j += 1
+    return tot
+
+
+def timeline_summary(trace: list) -> dict:
+    """Busy shares of one call's timeline (tiled_linear_get_trace): GEMMs,
+    the host->device and device->host copies, and both links at once under
+    a GEMM, as percentages of the call's span."""
+    if not trace:
+        return {}
+    t0 = min(e["start_ms"] for e in trace)
+    t1 = max(e["end_ms"] for e in trace)
+    span = max(t1 - t0, 1e-9)
+    gem = _union([(e["start_ms"], e["end_ms"]) for e in trace if e["kind"].endswith("gemm") or e["kind"] == "pass"])
+    h2d = _union([(e["start_ms"], e["end_ms"]) for e in trace if e["kind"] == "h2d"])
+    d2h = _union([(e["start_ms"], e["end_ms"]) for e in trace if e["kind"] == "d2h"])
+    busy = lambda u: sum(b - a for a, b in u)
+    both = _union([(max(a, c), min(b, d)) for a, b in h2d for c, d in d2h if min(b, d) > max(a, c)])
+    pct = lambda v: round(100.0 * v / span, 1)
+    return {"span_ms": round(span, 4), "gemm_busy_pct": pct(busy(gem)), "h2d_busy_pct": pct(busy(h2d)),
+            "d2h_busy_pct": pct(busy(d2h)), "both_links_under_gemm_pct": pct(_overlap(both, gem)),
+            "copy_outside_gemm_pct": pct(busy(_union(h2d + d2h)) - _overlap(_union(h2d + d2h), gem))}
+
+
 def disk_bandwidth(path: str, nbytes: int, threads: int = 4, chunk: int = 16 << 20) -> tuple:
     """Direct-I/O write then read bandwidth (GB/s) of a scratch file of
     `nbytes` at `path`, in `chunk` requests spread over `threads` threads
@@ -793,6 +837,12 @@ def run_ours(args, cfg, dist: Dist):
     launches = args.steps * (st["fwd_launches"] + st["bwd_launches"])
     n_dx = max(st["bwd_launches"] - N, 1)  # dX launches per backward (tile groups)
 
+    # --- the last timed call's launch and copy timeline ------------------------
+    trace_f, trace_b = op.trace(False), op.trace(True)
+    if args.trace_out and dist.rank == 0:
+        with open(args.trace_out, "w") as f:
+            json.dump({"workload": cfg["workload"], "forward": trace_f, "backward": trace_b}, f)
+
     # --- per-kernel averages over the timed region ---------------------------
     fc, bc = max(st["fwd_timed_calls"], 1), max(st["bwd_timed_calls"], 1)
     op.set_timing(1)
@@ -903,6 +953,9 @@ def run_ours(args, cfg, dist: Dist):
         out["exposed_copy_pct"] = exposed["exposed_copy_pct"]
         out["copy_overlap"] = exposed
     out["roofline"] = roofline
+    out["timeline"] = {"forward": timeline_summary(trace_f), "backward": timeline_summary(trace_b),
+                       "source": "CUDA events around every launch and copy of the last timed call "
+                                 "(tiled_linear_get_trace)"}
     out["engine_stats_last_step"] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in st.items()
                                      if not k.startswith("sum_")}
     out["clocks"] = clocks
@@ -1114,6 +1167,8 @@ def main():
     ap.add_argument("--skip-aux", action="store_true",
                     help="skip the link / copy-only / resident / e2e measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace-out", default=None,
+                    help="write the last timed forward and backward call's launch / copy timeline (JSON)")
     ap.add_argument("--tier-dir", default=os.environ.get("TMPDIR", "/tmp"),
                     help="directory for the file tier's W and dW files (the file_tier measurement)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -223,6 +223,34 @@ const char *tiled_linear_last_error(const tl_handle *h);
  * if a kernel gave up waiting. */
 tl_status tiled_linear_get_stats(tl_handle *h, void *tl_stats_out);
 
+/* Timeline of the last timed forward (backward = 0) or backward call: every
+ * GEMM launch and every tile copy that call made, with its start and end in
+ * milliseconds from the call's start on its `stream`, from the CUDA events the
+ * library records on the stream that ran it (the copy engines' view that a
+ * system trace would give).
+ *  kind: TL_TRACE_FWD_GEMM / _DW_GEMM / _DX_GEMM (a dX launch over a group of
+ *        tiles is listed under the group's lowest tile), TL_TRACE_H2D (a W
+ *        tile into the ring; tiles a backward reused from the ring have none),
+ *        TL_TRACE_D2H (a dW tile out), TL_TRACE_PASS (a whole persistent pass).
+ *  tile: the tile's index in the handle's order (a chain's operators follow
+ *        each other), -1 for a pass.
+ * Events are listed GEMMs first, in launch order, then copies in fetch order.
+ * A copy can start before the call does (a negative start): a weight fetch
+ * waits only for its ring slot, not for earlier work on `stream`.
+ * Writes min(*count, capacity) events to out and sets *count to the number
+ * there are (0 if no call of that direction was timed).  Waits for that call
+ * to finish.  Errors: TL_ERR_INVALID (null handle / count, negative
+ * capacity, null out with capacity > 0), TL_ERR_CUDA. */
+enum { TL_TRACE_FWD_GEMM = 0, TL_TRACE_DW_GEMM = 1, TL_TRACE_DX_GEMM = 2, TL_TRACE_H2D = 3, TL_TRACE_D2H = 4,
+       TL_TRACE_PASS = 5 };
+typedef struct {
+    int32_t kind;
+    int32_t tile;
+    float start_ms, end_ms;
+} tl_trace_event;
+tl_status tiled_linear_get_trace(tl_handle *h, int32_t backward, tl_trace_event *out, int32_t capacity,
+                                 int32_t *count);
+
 /* Wait for every recorded call to finish and zero the sum_* counters. */
 tl_status tiled_linear_reset_stats(tl_handle *h);
 

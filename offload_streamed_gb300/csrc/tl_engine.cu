@@ -145,6 +145,7 @@ constexpr int kTimingRing = 16;
 struct CallSlot {
     cudaEvent_t start = nullptr, end = nullptr;
     std::vector<cudaEvent_t> ev[8];
+    std::vector<char> dx_at;  // backward: a dX launch closed a tile group at this position
     bool pending = false;  // recorded, not yet harvested
     bool harvested = false;
     int32_t nk = 0;        // kernel spans recorded (N per-tile launches, or 1 pass)
@@ -276,6 +277,7 @@ tl_status create_phase(tl_handle* h, Phase& p, int n, bool backward) {
     p.backward = backward;
     p.ring.resize(kTimingRing);
     for (auto& c : p.ring) {
+        c.dx_at.assign(size_t(n), 0);
         TL_TRY(h, cudaEventCreate(&c.start));
         TL_TRY(h, cudaEventCreate(&c.end));
         for (int k = 0; k < 8; ++k) {
@@ -1093,6 +1095,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
                 pend.push_back(sl);
                 if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[2][jg], cs));
                 if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
+                t.dx_at[size_t(jg)] = 0;
                 continue;
             }
             // dX (+)= sum over the group's tiles i, i+1, .. of dY_i W_i^T, fp32;
@@ -1122,6 +1125,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             gx.accumulate = dx_launches > 0;
             gx.err = h->err_dev;
             if ((st = launch(h, gx, cs)) != TL_OK) return st;
+            t.dx_at[size_t(jg)] = 1;
             ++dx_launches;
             ++launches;
             if (t.timed) TL_TRY(h, cudaEventRecord(t.ev[3][jg], cs));
@@ -1426,6 +1430,41 @@ tl_status tiled_linear_destroy(tl_handle* h) {
 const char* tiled_linear_last_error(const tl_handle* h) {
     if (!h) return g_create_error.c_str();
     return h->msg.c_str();
+}
+
+tl_status tiled_linear_get_trace(tl_handle* h, int32_t backward, tl_trace_event* out, int32_t capacity,
+                                 int32_t* count) {
+    if (!h || !count || capacity < 0 || (capacity > 0 && !out)) return TL_ERR_INVALID;
+    *count = 0;
+    DeviceGuard guard(h->device);
+    Phase& p = backward ? h->bwd : h->fwd;
+    tl_status st = harvest_all(h, p);
+    if (st != TL_OK) return st;
+    if (p.last < 0) return TL_OK;
+    const CallSlot& c = p.ring[size_t(p.last)];
+    int32_t n = 0;
+    auto add = [&](int32_t kind, int32_t tile, cudaEvent_t a, cudaEvent_t b) {
+        const float t0 = span_ms(c.start, a), t1 = span_ms(c.start, b);
+        if (n < capacity) out[n] = tl_trace_event{kind, tile, t0, t1};
+        ++n;
+    };
+    const int NT = h->n_total;
+    if (c.nk == 1 && NT > 1) {  // one persistent launch for the pass
+        add(TL_TRACE_PASS, -1, c.ev[0][0], c.ev[1][0]);
+    } else {
+        for (int j = 0; j < c.nk; ++j) {
+            const int tile = backward ? NT - 1 - j : j;
+            add(backward ? TL_TRACE_DW_GEMM : TL_TRACE_FWD_GEMM, tile, c.ev[0][j], c.ev[1][j]);
+            if (backward && c.dx_at[size_t(j)]) add(TL_TRACE_DX_GEMM, tile, c.ev[2][j], c.ev[3][j]);
+        }
+    }
+    for (int j = 0; j < NT; ++j) {
+        const int tile = backward ? NT - 1 - j : j;
+        if (!backward || j >= c.reused) add(TL_TRACE_H2D, tile, c.ev[4][j], c.ev[5][j]);  // reused: no copy
+        if (backward) add(TL_TRACE_D2H, tile, c.ev[6][j], c.ev[7][j]);
+    }
+    *count = n;
+    return TL_OK;
 }
 
 tl_status tiled_linear_get_stats(tl_handle* h, void* out_v) {

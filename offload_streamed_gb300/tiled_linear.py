@@ -63,6 +63,15 @@ class tl_file_stats(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+TL_TRACE_FWD_GEMM, TL_TRACE_DW_GEMM, TL_TRACE_DX_GEMM, TL_TRACE_H2D, TL_TRACE_D2H, TL_TRACE_PASS = range(6)
+TRACE_KINDS = {0: "fwd_gemm", 1: "dw_gemm", 2: "dx_gemm", 3: "h2d", 4: "d2h", 5: "pass"}
+
+
+class tl_trace_event(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("tile", ctypes.c_int32),
+                ("start_ms", ctypes.c_float), ("end_ms", ctypes.c_float)]
+
+
 class tl_adam_config(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("threads", ctypes.c_int32)]
@@ -112,6 +121,8 @@ def load():
         L.tiled_linear_last_error.restype = ctypes.c_char_p
         L.tiled_linear_get_stats.argtypes = [vp, vp]
         L.tiled_linear_get_stats.restype = st
+        L.tiled_linear_get_trace.argtypes = [vp, i32, vp, i32, ctypes.POINTER(i32)]
+        L.tiled_linear_get_trace.restype = st
         L.tiled_linear_reset_stats.argtypes = [vp]
         L.tiled_linear_reset_stats.restype = st
         L.tiled_linear_set_tile_reuse.argtypes = [vp, i32]
@@ -226,6 +237,19 @@ def tiled_linear_get_stats(h: int) -> dict:
     s = tl_stats()
     _check(load().tiled_linear_get_stats(h, ctypes.byref(s)), "tiled_linear_get_stats", h)
     return s.as_dict()
+
+
+def tiled_linear_get_trace(h: int, backward: bool) -> list:
+    """The last timed forward / backward call's launches and copies: a list of
+    {"kind", "tile", "start_ms", "end_ms"} (see include/tiled_linear.h)."""
+    n = ctypes.c_int32(0)
+    _check(load().tiled_linear_get_trace(h, 1 if backward else 0, None, 0, ctypes.byref(n)),
+           "tiled_linear_get_trace", h)
+    buf = (tl_trace_event * max(n.value, 1))()
+    _check(load().tiled_linear_get_trace(h, 1 if backward else 0, buf, n.value, ctypes.byref(n)),
+           "tiled_linear_get_trace", h)
+    return [{"kind": TRACE_KINDS[e.kind], "tile": e.tile, "start_ms": e.start_ms, "end_ms": e.end_ms}
+            for e in buf[:n.value]]
 
 
 def tiled_linear_reset_stats(h: int) -> None:
@@ -452,6 +476,10 @@ class TiledLinear:
     def reset_stats(self) -> None:
         tiled_linear_reset_stats(self.handle)
 
+    def trace(self, backward: bool) -> list:
+        """Launch and copy timeline of the last timed forward / backward call."""
+        return tiled_linear_get_trace(self.handle, backward)
+
     def set_tile_reuse(self, enable: bool = True) -> None:
         """Let backward calls take the tiles still resident from the calls
         before them (W must not change in between)."""
@@ -568,6 +596,10 @@ class TiledLinearChain:
 
     def reset_stats(self) -> None:
         tiled_linear_reset_stats(self.handle)
+
+    def trace(self, backward: bool) -> list:
+        """Launch and copy timeline of the last timed forward / backward call."""
+        return tiled_linear_get_trace(self.handle, backward)
 
     def set_tile_reuse(self, enable: bool = True) -> None:
         tiled_linear_set_tile_reuse(self.handle, enable)

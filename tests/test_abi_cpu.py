@@ -111,11 +111,20 @@ def test_resident_gemm_argument_checks(tl):
     assert lib.tiled_linear_gemm_dx(64, 64, 64, 258, 64, 256, 64, 256, 64, 0, 256, None) == tl.TL_ERR_INVALID
 
 
+def test_trace_argument_checks(tl):
+    lib = tl.load()
+    n = ctypes.c_int32(5)
+    assert lib.tiled_linear_get_trace(None, 0, None, 0, ctypes.byref(n)) == tl.TL_ERR_INVALID
+    assert lib.tiled_linear_get_trace(256, 0, None, 0, None) == tl.TL_ERR_INVALID  # null count
+    assert lib.tiled_linear_get_trace(256, 0, None, -1, ctypes.byref(n)) == tl.TL_ERR_INVALID
+    assert lib.tiled_linear_get_trace(256, 0, None, 4, ctypes.byref(n)) == tl.TL_ERR_INVALID  # null out
+
+
 def test_null_handle_tile_reuse(tl):
     assert tl.load().tiled_linear_set_tile_reuse(None, 1) == tl.TL_ERR_STATE
 
 
-@pytest.mark.parametrize("struct", ["tl_stats", "tl_file_stats", "tl_adam_config"])
+@pytest.mark.parametrize("struct", ["tl_stats", "tl_file_stats", "tl_adam_config", "tl_trace_event"])
 def test_stats_struct_layout_matches_the_header(tl, tmp_path, struct):
     """The binding's structs mirror the C structs field by field: a C program
     built against include/tiled_linear.h prints sizeof and every offsetof."""
