@@ -603,21 +603,26 @@ def _overlap(x, y):
 def timeline_summary(trace: list) -> dict:
     """Busy shares of one call's timeline (tiled_linear_get_trace): GEMMs,
     the host->device and device->host copies, and both links at once under
-    a GEMM, as percentages of the call's span."""
+    a GEMM, as percentages of the call's span.  The span starts at the call's
+    start (time 0): copies fetched earlier, under the previous call's GEMMs,
+    are clipped to it."""
     if not trace:
         return {}
-    t0 = min(e["start_ms"] for e in trace)
     t1 = max(e["end_ms"] for e in trace)
-    span = max(t1 - t0, 1e-9)
-    gem = _union([(e["start_ms"], e["end_ms"]) for e in trace if e["kind"].endswith("gemm") or e["kind"] == "pass"])
-    h2d = _union([(e["start_ms"], e["end_ms"]) for e in trace if e["kind"] == "h2d"])
-    d2h = _union([(e["start_ms"], e["end_ms"]) for e in trace if e["kind"] == "d2h"])
+    span = max(t1, 1e-9)
+    sel = lambda f: _union([(max(e["start_ms"], 0.0), e["end_ms"]) for e in trace
+                            if f(e["kind"]) and e["end_ms"] > 0.0])
+    gem = sel(lambda k: k.endswith("gemm") or k == "pass")
+    h2d = sel(lambda k: k == "h2d")
+    d2h = sel(lambda k: k == "d2h")
+    early = sum(1 for e in trace if e["kind"] == "h2d" and e["start_ms"] < 0.0)
     busy = lambda u: sum(b - a for a, b in u)
     both = _union([(max(a, c), min(b, d)) for a, b in h2d for c, d in d2h if min(b, d) > max(a, c)])
     pct = lambda v: round(100.0 * v / span, 1)
     return {"span_ms": round(span, 4), "gemm_busy_pct": pct(busy(gem)), "h2d_busy_pct": pct(busy(h2d)),
             "d2h_busy_pct": pct(busy(d2h)), "both_links_under_gemm_pct": pct(_overlap(both, gem)),
-            "copy_outside_gemm_pct": pct(busy(_union(h2d + d2h)) - _overlap(_union(h2d + d2h), gem))}
+            "copy_outside_gemm_pct": pct(busy(_union(h2d + d2h)) - _overlap(_union(h2d + d2h), gem)),
+            "copies_started_before_the_call": early}
 
 
 def disk_bandwidth(path: str, nbytes: int, threads: int = 4, chunk: int = 16 << 20) -> tuple:
