@@ -701,10 +701,10 @@ def run_file_tier(tl, cfg, w, x, y, dy, dx, steps: int, dist: Dist, flops_step: 
         sec = dist.max((time.perf_counter() - t0) / steps)
         f1 = op.file_stats()
         op.close()
-    except tl.TiledLinearError as e:
-        return {"unavailable": str(e)}
+    except (tl.TiledLinearError, OSError) as e:  # e.g. a filesystem without direct I/O
+        return {"unavailable": f"{type(e).__name__}: {e}"}
     finally:
-        for f in (wp, dwp):
+        for f in (wp, dwp, os.path.join(work, "probe.bin")):
             if os.path.exists(f):
                 os.unlink(f)
         os.rmdir(work)
