@@ -778,6 +778,21 @@ def run_ffn_chain(tl, cfg, x, y_up, dx, seed: int, steps: int, dist: Dist) -> di
 
 
 # ----------------------------------------------------------------------------
+def _extension(fn) -> dict:
+    """Run one extension measurement; a failure there (a pinned allocation
+    the host refuses, a filesystem without direct I/O) is reported in its own
+    object and never costs the method's measurement.  A CUDA failure is not
+    caught: it can leave the context unusable, and then nothing after it is
+    trustworthy."""
+    from offload_streamed_gb300 import tiled_linear as tl
+    try:
+        return fn()
+    except (tl.TiledLinearError, OSError, MemoryError) as e:
+        if isinstance(e, tl.TiledLinearError) and e.status in (tl.TL_ERR_CUDA, tl.TL_ERR_TIMEOUT):
+            raise
+        return {"unavailable": f"{type(e).__name__}: {e}"}
+
+
 def run_ours(args, cfg, dist: Dist):
     import torch
 
@@ -1006,15 +1021,18 @@ def run_ours(args, cfg, dist: Dist):
 
     # --- training step with the Adam update on the host CPU (overlapped) -------
     if not args.skip_aux and not persistent:
-        out["host_adam"] = run_host_adam(tl, op, x, y, dy, dx, max(3, min(args.steps, 10)), dist, flops_step)
+        out["host_adam"] = _extension(lambda: run_host_adam(tl, op, x, y, dy, dx, max(3, min(args.steps, 10)), dist,
+                                                            flops_step))
 
     # --- the FFN chain (up- then down-projection) through one prefetcher -------
     if not args.skip_aux and not persistent and M % K == 0:
-        out["ffn_chain"] = run_ffn_chain(tl, cfg, x, y, dx, args.seed, max(3, min(args.steps, 20)), dist)
+        out["ffn_chain"] = _extension(lambda: run_ffn_chain(tl, cfg, x, y, dx, args.seed, max(3, min(args.steps, 20)),
+                                                            dist))
 
     # --- W and dW one tier further down: files on the box's disk -----------------
     if not args.skip_aux and not persistent:
-        out["file_tier"] = run_file_tier(tl, cfg, w, x, y, dy, dx, 3, dist, flops_step, peaks, args.tier_dir)
+        out["file_tier"] = _extension(lambda: run_file_tier(tl, cfg, w, x, y, dy, dx, 3, dist, flops_step, peaks,
+                                                            args.tier_dir))
 
     # --- CPU oracle baseline ----------------------------------------------------
     if want_cpu:
