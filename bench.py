@@ -778,13 +778,16 @@ def run_ffn_chain(tl, cfg, x, y_up, dx, seed: int, steps: int, dist: Dist) -> di
 
 
 # ----------------------------------------------------------------------------
-def _extension(fn) -> dict:
+def _extension(fn, dist: Dist) -> dict:
     """Run one extension measurement; a failure there (a pinned allocation
     the host refuses, a filesystem without direct I/O) is reported in its own
     object and never costs the method's measurement.  A CUDA failure is not
     caught: it can leave the context unusable, and then nothing after it is
-    trustworthy."""
+    trustworthy.  With several ranks nothing is caught either: a rank that
+    went on would leave the others waiting in the extension's collectives."""
     from offload_streamed_gb300 import tiled_linear as tl
+    if dist.world > 1:
+        return fn()
     try:
         return fn()
     except (tl.TiledLinearError, OSError, MemoryError) as e:
@@ -1022,17 +1025,17 @@ def run_ours(args, cfg, dist: Dist):
     # --- training step with the Adam update on the host CPU (overlapped) -------
     if not args.skip_aux and not persistent:
         out["host_adam"] = _extension(lambda: run_host_adam(tl, op, x, y, dy, dx, max(3, min(args.steps, 10)), dist,
-                                                            flops_step))
+                                                            flops_step), dist)
 
     # --- the FFN chain (up- then down-projection) through one prefetcher -------
     if not args.skip_aux and not persistent and M % K == 0:
         out["ffn_chain"] = _extension(lambda: run_ffn_chain(tl, cfg, x, y, dx, args.seed, max(3, min(args.steps, 20)),
-                                                            dist))
+                                                            dist), dist)
 
     # --- W and dW one tier further down: files on the box's disk -----------------
     if not args.skip_aux and not persistent:
         out["file_tier"] = _extension(lambda: run_file_tier(tl, cfg, w, x, y, dy, dx, 3, dist, flops_step, peaks,
-                                                            args.tier_dir))
+                                                            args.tier_dir), dist)
 
     # --- CPU oracle baseline ----------------------------------------------------
     if want_cpu:
