@@ -702,6 +702,8 @@ def run_file_tier(tl, cfg, w, x, y, dy, dx, steps: int, dist: Dist, flops_step: 
         f1 = op.file_stats()
         op.close()
     except (tl.TiledLinearError, OSError) as e:  # e.g. a filesystem without direct I/O
+        if dist.world > 1:  # the other ranks would wait at this extension's barrier
+            raise
         return {"unavailable": f"{type(e).__name__}: {e}"}
     finally:
         for f in (wp, dwp, os.path.join(work, "probe.bin")):
