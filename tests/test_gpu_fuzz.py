@@ -31,7 +31,7 @@ def _draw(rng):
     return T, K, N * Mi, N, d
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_single_operator_schedules(tl, seed):
     rng = np.random.default_rng(1000 + seed)
     T, K, M, N, d = _draw(rng)
@@ -61,7 +61,7 @@ def test_random_single_operator_schedules(tl, seed):
     dw.close()
 
 
-@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("seed", range(10))
 def test_random_chains(tl, seed):
     rng = np.random.default_rng(2000 + seed)
     L = int(rng.integers(1, 4))
@@ -101,7 +101,7 @@ def test_random_chains(tl, seed):
         b.close()
 
 
-@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("seed", range(6))
 def test_random_file_tier(tl, tmp_path, seed):
     """Random shapes, depths, host slots, I/O threads, reuse and call counts
     through the file tier: bit-identical to the host-memory path (which the
