@@ -326,8 +326,8 @@ tl_status tiled_linear_adam_update(const tl_adam_config *cfg, int64_t step, int6
  * forward / backward may therefore block the calling thread.  Results are
  * bit-identical to calling tiled_linear_adam_update tile by tile after the
  * backward completes.  Host waits give up after 600 s with TL_ERR_TIMEOUT.
- * Errors: TL_ERR_INVALID (arguments, persistent mode, accumulate without an
- * accumulator), TL_ERR_STATE (no backward since the last optimizer call, or
+ * Errors: TL_ERR_INVALID (arguments, persistent mode, a handle whose W and
+ * dW are in files, accumulate without an accumulator), TL_ERR_STATE (no backward since the last optimizer call, or
  * an optimizer already attached), TL_ERR_CUDA, TL_ERR_TIMEOUT. */
 typedef struct tl_optimizer tl_optimizer;
 tl_status tiled_linear_optimizer_create(tl_optimizer **out, tl_handle *h, const tl_adam_config *cfg,
