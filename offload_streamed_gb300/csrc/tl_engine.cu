@@ -20,6 +20,15 @@
 // accumulates dX with the W_i tile (pwwt.cn/news/5430303, "关键技术三",
 // 后向传播中的重叠: gradients go back to slow memory while later operators
 // compute).
+//
+// Also here: dX over groups of tiles that sit in the ring together; the dW
+// staging slots lent to the forward as extra fetch slots; tile reuse across
+// calls; chains of operators through one ring; the hooks of the host
+// optimizer (tl_optimizer: host waits before a tile's W is copied in or its
+// dW overwritten) and of the file tier (tl_filetier: a tile's bytes pass
+// through pinned host slots between a file and the same copies); the sampled
+// per-launch and per-copy timing and the call timeline built from it; and
+// the persistent-pass mode (tl_pass.cu).
 #include "tiled_linear.h"
 #include "tl_cast.h"
 #include "tl_filetier.h"
