@@ -382,7 +382,9 @@ tl_status tiled_linear_chain_create(tl_handle **out, int32_t L, const int64_t *d
 tl_status tiled_linear_chain_forward(tl_handle *h, int64_t T, const void *x_dev,
                                      void *const *y_dev, void *stream);
 
-/* Device scratch bytes the chain backward needs: an fp32 and a bf16 buffer of
+/* Device scratch bytes the chain backward needs: an fp32 buffer and, for the
+ * dY between operators, one bf16 buffer (two for L >= 3, so that a middle
+ * operator writes the next dY beside the one it reads), each of
  * T x max(dims[1..L-1]) elements (0 for L = 1). */
 size_t tiled_linear_chain_scratch_bytes(int64_t T, int32_t L, const int64_t *dims);
 
@@ -432,6 +434,20 @@ tl_status tiled_linear_gemm_dx(int64_t T, int64_t K, int64_t n,
                                const void *w_dev, int64_t ldw,
                                float *dx_dev, int64_t lddx, int32_t accumulate,
                                int32_t *err_dev, void *stream);
+
+/* dx[T, K] (bf16, ld lddx) = bf16(addend[T, K] + dy[T, n] . w[K, n]^T): the
+ * product as tiled_linear_gemm_dx computes it in fp32, plus the fp32 addend
+ * (ld ld_add, a multiple of 8 >= K; NULL: no addend), rounded to nearest even
+ * once.  A chain's last dX launch per operator writes the previous operator's
+ * dY this way (operators in sequence, each tiled as ZeRO-Infinity's
+ * "Memory-centric tiling" splits one).  The result equals tiled_linear_gemm_dx
+ * with accumulate = 1 into a copy of the addend, then rounded to bf16. */
+tl_status tiled_linear_gemm_dx_bf16(int64_t T, int64_t K, int64_t n,
+                                    const void *dy_dev, int64_t lddy,
+                                    const void *w_dev, int64_t ldw,
+                                    const float *addend_dev, int64_t ld_add,
+                                    void *dx_dev, int64_t lddx,
+                                    int32_t *err_dev, void *stream);
 
 /* Self-test of the kernels' failure path.  Launches the forward GEMM kernel
  * on a 128 x 256 x 64 problem with every operand load withheld and every

@@ -29,7 +29,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompil
 # Extra flags of single units: the host optimizer's row loop vectorizes its
 # square roots only without errno semantics.
 UNIT_FLAGS = {"tl_adam.cpp": ["-Xcompiler", "-fno-math-errno"]}
-UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_cast.cu", "tl_adam.cpp", "tl_filetier.cpp",
+UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_adam.cpp", "tl_filetier.cpp",
          "tl_optimizer.cpp"]
 
 

@@ -30,7 +30,6 @@
 // per-launch and per-copy timing and the call timeline built from it; and
 // the persistent-pass mode (tl_pass.cu).
 #include "tiled_linear.h"
-#include "tl_cast.h"
 #include "tl_filetier.h"
 #include "tl_gemm.h"
 #include "tl_optimizer.h"
@@ -949,10 +948,13 @@ tl_status forward_tiles(tl_handle* h, int64_t T, const void* x, void* const* ys,
 // Backward, operators in reverse and each one's tiles in descending order:
 //   dW_{l,i} = X_l^T . dY_l[:, tile i] -> staging slot -> host (d2h stream)
 //   dX_l (+)= dY_l[:, tile i] . W_{l,i}^T in fp32 (tile groups, see dx_group)
-// dY_{L-1} = dy; for l < L-1, dY_l = bf16(dX_{l+1}) (cast on the caller's
-// stream into scr_dy), dX_l for l >= 1 accumulates in scr_dx, dX_0 in dx.
+// dY_{L-1} = dy; for l < L-1, dY_l = bf16(dX_{l+1}): dX_l for l >= 1
+// accumulates in scr_dx, and operator l's last dX launch adds its share to
+// the fp32 sum of the earlier ones and writes the bf16 RNE of the total as
+// dY_{l-1}, into scr_dy[(L - 1 - l) % 2] (two buffers, so that an operator
+// never writes the dY it reads).  dX_0 goes to dx.
 tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* const* ys, const void* dy,
-                         float* dx, float* scr_dx, void* scr_dy, cudaStream_t cs) {
+                         float* dx, float* scr_dx, void* const* scr_dy, cudaStream_t cs) {
     tl_status st;
     const int L = int(h->ops.size());
     withdraw_staging(h);
@@ -1020,7 +1022,7 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
         const Op& o = h->ops[size_t(l)];
         const Shape& s = o.s;
         const void* xl = l == 0 ? x : ys[l - 1];
-        const void* dyl = l == L - 1 ? dy : scr_dy;
+        const void* dyl = l == L - 1 ? dy : scr_dy[(L - 2 - l) % 2];
         float* dxl = l == 0 ? dx : scr_dx;
         const size_t tb = tile_bytes(s.K, s.Mi);
         // dX is accumulated over groups of tiles (i+g-1, ..., i) -- one
@@ -1128,11 +1130,18 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
                 gx.k_seg = s.Mi;
                 for (size_t jj = 0; jj < grp.size(); ++jj) gx.bseg[jj] = h->slot[size_t(grp[jj])];
             }
-            gx.d = dxl;
             gx.ldd = s.K;
-            gx.out = tl::OutKind::F32;
-            gx.accumulate = dx_launches > 0;
             gx.err = h->err_dev;
+            if (l > 0 && j + 1 == s.N) {  // the operator's last dX launch: the previous one's dY in bf16
+                gx.d = scr_dy[(L - 1 - l) % 2];
+                gx.out = tl::OutKind::BF16;
+                gx.addend = dx_launches > 0 ? dxl : nullptr;
+                gx.ld_addend = s.K;
+            } else {
+                gx.d = dxl;
+                gx.out = tl::OutKind::F32;
+                gx.accumulate = dx_launches > 0;
+            }
             if ((st = launch(h, gx, cs)) != TL_OK) return st;
             t.dx_at[size_t(jg)] = 1;
             ++dx_launches;
@@ -1145,12 +1154,6 @@ tl_status backward_tiles(tl_handle* h, int64_t T, const void* x, const void* con
             TL_TRY(h, cudaEventRecord(h->ev_free[sl], cs));
             h->slot_q.push_back(sl);
             pend.clear();
-        }
-        if (l > 0) {  // dY of the operator before: bf16 RNE of this dX
-            std::string why;
-            if (tl::cast_f32_bf16(scr_dx, scr_dy, T * s.K, h->num_sms, cs, &why) != cudaSuccess)
-                return fail(h, TL_ERR_CUDA, "dX -> dY cast: " + why);
-            ++launches;
         }
     }
     // dW on the host is complete when `stream` is.
@@ -1327,7 +1330,8 @@ size_t tiled_linear_chain_scratch_bytes(int64_t T, int32_t L, const int64_t* dim
     int64_t inner = 0;
     for (int l = 1; l < L; ++l) inner = std::max(inner, dims[l]);
     if (inner == 0) return 0;
-    return align_up(size_t(T) * size_t(inner) * 4, kAlign) + align_up(size_t(T) * size_t(inner) * 2, kAlign);
+    const size_t dy_bufs = L >= 3 ? 2 : 1;  // dY buffers: an operator between two others reads one, writes the other
+    return align_up(size_t(T) * size_t(inner) * 4, kAlign) + dy_bufs * align_up(size_t(T) * size_t(inner) * 2, kAlign);
 }
 
 tl_status tiled_linear_chain_forward(tl_handle* h, int64_t T, const void* x_dev, void* const* y_dev,
@@ -1354,7 +1358,7 @@ tl_status tiled_linear_chain_backward(tl_handle* h, int64_t T, const void* x_dev
     if (h->single_api) return fail(h, TL_ERR_INVALID, "a single-operator handle runs tiled_linear_backward");
     const int L = int(h->ops.size());
     float* scr_dx = nullptr;
-    void* scr_dy = nullptr;
+    void* scr_dy[2] = {nullptr, nullptr};
     if (T > 0) {
         if (!x_dev || !dy_dev || !dx_dev || misaligned(x_dev) || misaligned(dy_dev) || misaligned(dx_dev))
             return fail(h, TL_ERR_INVALID, "x, dy and dx must be non-null and 16-byte aligned");
@@ -1373,7 +1377,8 @@ tl_status tiled_linear_chain_backward(tl_handle* h, int64_t T, const void* x_dev
             int64_t inner = 0;
             for (int l = 1; l < L; ++l) inner = std::max(inner, dims[size_t(l)]);
             scr_dx = static_cast<float*>(scratch_dev);
-            scr_dy = static_cast<uint8_t*>(scratch_dev) + align_up(size_t(T) * size_t(inner) * 4, kAlign);
+            scr_dy[0] = static_cast<uint8_t*>(scratch_dev) + align_up(size_t(T) * size_t(inner) * 4, kAlign);
+            if (L >= 3) scr_dy[1] = static_cast<uint8_t*>(scr_dy[0]) + align_up(size_t(T) * size_t(inner) * 2, kAlign);
         }
     }
     DeviceGuard guard(h->device);
@@ -1783,6 +1788,28 @@ tl_status tiled_linear_gemm_dx(int64_t T, int64_t K, int64_t n, const void* dy_d
     g.ldd = lddx;
     g.out = tl::OutKind::F32;
     g.accumulate = accumulate != 0;
+    g.err = err_dev;
+    return raw_launch(g, stream);
+}
+
+tl_status tiled_linear_gemm_dx_bf16(int64_t T, int64_t K, int64_t n, const void* dy_dev, int64_t lddy,
+                                    const void* w_dev, int64_t ldw, const float* addend_dev, int64_t ld_add,
+                                    void* dx_dev, int64_t lddx, int32_t* err_dev, void* stream) {
+    tl::GemmDesc g;
+    g.m_dim = T;
+    g.n_dim = K;
+    g.k_dim = n;
+    g.a = dy_dev;
+    g.lda = lddy;
+    g.a_mn_major = false;
+    g.b = w_dev;
+    g.ldb = ldw;
+    g.b_mn_major = false;
+    g.d = dx_dev;
+    g.ldd = lddx;
+    g.out = tl::OutKind::BF16;
+    g.addend = addend_dev;
+    g.ld_addend = ld_add;
     g.err = err_dev;
     return raw_launch(g, stream);
 }

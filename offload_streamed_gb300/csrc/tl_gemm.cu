@@ -53,6 +53,8 @@ struct KParams {
     void* d;
     int64_t ldd;
     int32_t accumulate;
+    const float* addend;  // bf16 input-gradient kind: D = bf16(addend + A.B) (nullptr: no addend)
+    int64_t ld_add;
     int32_t withhold_loads;
     int32_t* err;
     uint32_t* tile_counter;  // dynamic schedule (nullptr: static round robin)
@@ -298,6 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * kBlockN;
             if constexpr (OUT_F32) {
                 epi_f32_tma(&map_d, t_row, epi0, buf, nchunks, n0, row0, lane, p.accumulate != 0);
+            } else if constexpr (!A_MN && !B_MN) {  // dX rounded to bf16, after the addend if any
+                if (p.addend)
+                    epi_bf16_add_tma(&map_d, t_row, epi0, buf, nchunks, n0, row0, lane, p.addend, p.ld_add,
+                                     p.m_dim, p.n_dim);
+                else
+                    epi_bf16_tma(&map_d, t_row, epi0, buf, nchunks, n0, row0, lane);
             } else {
                 epi_bf16_tma(&map_d, t_row, epi0, buf, nchunks, n0, row0, lane);
             }
@@ -394,6 +402,7 @@ cudaError_t dispatch(const GemmDesc& g, const CUtensorMap& ma, const CUtensorMap
     if (!g.a_mn_major && g.b_mn_major)
         return launch_one<false, true, false, PAIR>(ma, mb, md, segs, kp, grid, stream);
     if (g.a_mn_major && g.b_mn_major) return launch_one<true, true, false, PAIR>(ma, mb, md, segs, kp, grid, stream);
+    if (g.out == OutKind::BF16) return launch_one<false, false, false, PAIR>(ma, mb, md, segs, kp, grid, stream);
     return launch_one<false, false, true, PAIR>(ma, mb, md, segs, kp, grid, stream);
 }
 
@@ -461,8 +470,15 @@ std::string gemm_check(const GemmDesc& g) {
     const bool fwd = !g.a_mn_major && g.b_mn_major && g.out == OutKind::BF16;
     const bool dw = g.a_mn_major && g.b_mn_major && g.out == OutKind::BF16;
     const bool dx = !g.a_mn_major && !g.b_mn_major && g.out == OutKind::F32;
-    if (!(fwd || dw || dx)) return "unsupported operand-major / output combination";
+    const bool dx_bf16 = !g.a_mn_major && !g.b_mn_major && g.out == OutKind::BF16;
+    if (!(fwd || dw || dx || dx_bf16)) return "unsupported operand-major / output combination";
     if (g.accumulate && g.out != OutKind::F32) return "accumulate needs fp32 output";
+    if (g.addend) {
+        if (!dx_bf16) return "an addend needs the bf16 input-gradient kind";
+        if (!aligned16(g.addend)) return "addend pointer must be 16-byte aligned";
+        if (g.ld_addend % 8 || g.ld_addend < g.n_dim) return "addend leading dimension must be a multiple of 8 and >= n";
+        if (g.ld_addend * 4 >= (int64_t(1) << 40)) return "addend leading dimension too large";
+    }
     if (g.nseg < 1 || g.nseg > GemmDesc::kMaxSeg) return "nseg must be in 1..4";
     if (g.nseg > 1) {
         if (g.b_mn_major) return "B segments need a K-major B";
@@ -514,6 +530,8 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     kp.d = g.d;
     kp.ldd = g.ldd;
     kp.accumulate = g.accumulate ? 1 : 0;
+    kp.addend = g.addend;
+    kp.ld_add = g.ld_addend;
     kp.withhold_loads = g.withhold_loads ? 1 : 0;
     kp.err = g.err;
     kp.tile_counter = g.tile_counter;

@@ -7,6 +7,8 @@
 // All three run one persistent kernel template: bf16 operands fed by TMA into
 // a shared-memory ring, tcgen05 MMAs accumulating in fp32 in tensor memory,
 // and an epilogue that rounds to bf16 (K1, K3) or stores / adds fp32 (K2).
+// K2 may also round to bf16, after adding an fp32 addend: the last dX launch
+// of an operator in a chain writes the previous operator's dY directly.
 #pragma once
 #include <cstdint>
 #include <string>
@@ -40,6 +42,11 @@ struct GemmDesc {
     int64_t ldd = 0;
     OutKind out = OutKind::BF16;
     bool accumulate = false;  // F32 only: D += A.B
+    // BF16 output of the input-gradient kind (A and B K-major) only: with an
+    // addend, D = bf16(addend + A.B), addend fp32 [m_dim][ld_addend], the sum
+    // taken in fp32 and rounded once.
+    const float* addend = nullptr;
+    int64_t ld_addend = 0;
     int32_t* err = nullptr;   // device word for bounded-wait timeouts
     // Device word the CTAs draw output tiles from (dynamic schedule); zero
     // before the launch, and left zero by a launch that completes without a

@@ -174,6 +174,63 @@ __device__ __forceinline__ void epi_bf16_tma(const CUtensorMap* map, uint32_t t_
     }
 }
 
+// bf16 of (addend + accumulator), for a dX that is the next operator's dY:
+// each lane reads its own row of the fp32 addend (ld `ld_add`) with 16-byte
+// loads, issued before the chunk's TMEM loads so that the two latencies
+// overlap, adds it in fp32 (round to nearest, as a reduce-add in L2 would)
+// and rounds the sum to bf16 once.  Rows >= m_dim and columns >= n_dim read
+// no addend; the TMA store clips them.
+__device__ __forceinline__ void epi_bf16_add_tma(const CUtensorMap* map, uint32_t t_row, uint32_t epi0,
+                                                 uint32_t& buf, int nchunks, int col0, int row0, int lane,
+                                                 const float* addend, int64_t ld_add, int m_dim, int n_dim) {
+    const int row = row0 + lane;
+    const float* arow = addend + int64_t(row) * ld_add;
+    for (int c = 0; c < nchunks; ++c) {
+        const int cb = col0 + c * 64;
+        float a[64];
+        if (row < m_dim && cb + 64 <= n_dim) {
+            const float4* src = reinterpret_cast<const float4*>(arow + cb);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float4 f = __ldg(src + q);
+                a[4 * q] = f.x;
+                a[4 * q + 1] = f.y;
+                a[4 * q + 2] = f.z;
+                a[4 * q + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) a[e] = (row < m_dim && cb + e < n_dim) ? __ldg(arow + cb + e) : 0.0f;
+        }
+        uint32_t w[32];
+        uint32_t v[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            tmem_ld_32cols(t_row + uint32_t(c) * 64u + 32u * uint32_t(h), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                w[16 * h + j] = pack_bf16x2(__fadd_rn(a[32 * h + 2 * j], __uint_as_float(v[2 * j])),
+                                            __fadd_rn(a[32 * h + 2 * j + 1], __uint_as_float(v[2 * j + 1])));
+        }
+        const uint32_t sbuf = epi0 + buf * kEpiBuf;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used sbuf has read it
+        __syncwarp();
+        const uint32_t row_addr = sbuf + uint32_t(lane) * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(row_addr + ((uint32_t(j) ^ (uint32_t(lane) & 7u)) << 4), w[4 * j], w[4 * j + 1],
+                         w[4 * j + 2], w[4 * j + 3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, sbuf, cb, row0);
+            bulk_commit_group();
+        }
+        buf ^= 1u;
+    }
+}
+
 // fp32 through TMA: per 32-column chunk, tcgen05.ld of the lane's row into a
 // 128B-swizzled staging box (two per warp, alternating), and lane 0 issues a
 // TMA store of the 32 x 32 box at (col0 + 32c, row0) -- or, with `add`, a TMA

@@ -155,6 +155,8 @@ def load():
         L.tiled_linear_gemm_dw.restype = st
         L.tiled_linear_gemm_dx.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp, vp]
         L.tiled_linear_gemm_dx.restype = st
+        L.tiled_linear_gemm_dx_bf16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, vp]
+        L.tiled_linear_gemm_dx_bf16.restype = st
         L.tiled_linear_selftest_timeout.argtypes = [vp, sz, i64, vp]
         L.tiled_linear_selftest_timeout.restype = st
         L.tiled_linear_forward_static.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp]
@@ -358,6 +360,11 @@ def tiled_linear_gemm_dw(T, K, n, x, ldx, dy, lddy, dw, lddw, err, stream) -> No
 def tiled_linear_gemm_dx(T, K, n, dy, lddy, w, ldw, dx, lddx, accumulate, err, stream) -> None:
     _check(load().tiled_linear_gemm_dx(T, K, n, dy, lddy, w, ldw, dx, lddx, int(accumulate), err, stream),
            "tiled_linear_gemm_dx")
+
+
+def tiled_linear_gemm_dx_bf16(T, K, n, dy, lddy, w, ldw, addend, ld_add, dx, lddx, err, stream) -> None:
+    _check(load().tiled_linear_gemm_dx_bf16(T, K, n, dy, lddy, w, ldw, addend, ld_add, dx, lddx, err, stream),
+           "tiled_linear_gemm_dx_bf16")
 
 
 def tiled_linear_selftest_timeout(scratch_dev: int, scratch_bytes: int, timeout_ns: int, stream: int) -> None:

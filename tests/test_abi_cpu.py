@@ -109,6 +109,13 @@ def test_resident_gemm_argument_checks(tl):
     assert lib.tiled_linear_gemm_dw(64, 64, 64, 256, 60, 256, 64, 256, 64, 256, None) == tl.TL_ERR_INVALID
     assert lib.tiled_linear_gemm_dx(64, 64, 64, 256, 64, 256, 64, 256, 32, 0, 256, None) == tl.TL_ERR_INVALID
     assert lib.tiled_linear_gemm_dx(64, 64, 64, 258, 64, 256, 64, 256, 64, 0, 256, None) == tl.TL_ERR_INVALID
+    # the bf16 dX: a misaligned addend, an addend row shorter than K or not a
+    # multiple of 8 elements
+    dxb = lib.tiled_linear_gemm_dx_bf16
+    assert dxb(64, 64, 64, 256, 64, 256, 64, 264, 64, 256, 64, 256, None) == tl.TL_ERR_INVALID
+    assert dxb(64, 64, 64, 256, 64, 256, 64, 256, 56, 256, 64, 256, None) == tl.TL_ERR_INVALID
+    assert dxb(64, 64, 64, 256, 64, 256, 64, 256, 68, 256, 64, 256, None) == tl.TL_ERR_INVALID
+    assert dxb(64, 64, 64, None, 64, 256, 64, None, 0, 256, 64, 256, None) == tl.TL_ERR_INVALID
 
 
 def test_trace_argument_checks(tl):
@@ -182,7 +189,9 @@ def test_chain_workspace_and_scratch_bytes(tl):
         assert tl.tiled_linear_chain_workspace_bytes(1, [K, M], [N], d) == tl.tiled_linear_workspace_bytes(K, M, N, d)
     assert tl.tiled_linear_chain_workspace_bytes(2, [1024, 4096, 500], [4, 3], 1) == 0  # 500 % 3
     assert tl.tiled_linear_chain_workspace_bytes(0, [1024], [], 1) == 0
-    assert tl.tiled_linear_chain_scratch_bytes(100, 3, [64, 256, 128, 64]) == 100 * 256 * 4 + 100 * 256 * 2
+    # fp32 dX and one bf16 dY buffer; two dY buffers from three operators on
+    assert tl.tiled_linear_chain_scratch_bytes(100, 2, [64, 256, 64]) == 100 * 256 * 4 + 100 * 256 * 2
+    assert tl.tiled_linear_chain_scratch_bytes(100, 3, [64, 256, 128, 64]) == 100 * 256 * 4 + 2 * 100 * 256 * 2
     assert tl.tiled_linear_chain_scratch_bytes(100, 1, [64, 256]) == 0
 
 

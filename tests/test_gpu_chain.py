@@ -101,29 +101,33 @@ def test_chain_matches_oracle(tl, T, dims, n, d):
     assert r.stats["n_tiles"] == sum(n)
 
 
-def test_chain_composes_the_single_operator_calls(tl):
+@pytest.mark.parametrize("T,dims,n,d", [(200, [256, 768, 512], [3, 2], 1),
+                                        (136, [192, 512, 320, 384], [2, 5, 3], 2),
+                                        (64, [128, 256, 384, 128, 256], [1, 3, 2, 2], 1)])
+def test_chain_composes_the_single_operator_calls(tl, T, dims, n, d):
     """The chain's results are the single-operator calls applied in turn, bit
-    for bit: operator 1 on the chain's own Y_0, and operator 0's backward on
-    bf16 of operator 1's dX."""
-    T, dims, n, d = 200, [256, 768, 512], [3, 2], 1
+    for bit: operator l on the chain's own Y_{l-1}, and operator l's backward
+    on bf16 of operator l+1's dX.  With three or more operators the middle
+    ones read one dY buffer and write the other."""
     r = run_chain(tl, T, dims, n, d, seed=11)
-    ops = []
-    bufs = []
-    for l in range(2):
+    L = len(n)
+    ops, bufs = [], []
+    for l in range(L):
         K, M = dims[l], dims[l + 1]
         wb, dwb = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
         wb.tensor.view(n[l], K, M // n[l]).copy_(r.W[l].view(K, n[l], M // n[l]).permute(1, 0, 2))
         bufs += [wb, dwb]
         ops.append((tl.TiledLinear(K, M, n[l], d, wb, dwb, tile_major=True), dwb))
-    x, y0 = r.x.cuda(), r.ys[0].cuda()
-    y1 = ops[1][0].forward(y0)
-    dx1 = ops[1][0].backward(y0, r.dy.cuda())
-    dx0 = ops[0][0].backward(x, dx1.to(torch.bfloat16))
+    xs = [r.x.cuda()] + [y.cuda() for y in r.ys[:-1]]
+    for l in range(L):
+        assert _same(ops[l][0].forward(xs[l]).cpu(), r.ys[l]), l
+    g = r.dy.cuda()
+    for l in range(L - 1, -1, -1):
+        dx = ops[l][0].backward(xs[l], g)
+        g = dx.to(torch.bfloat16)
     torch.cuda.synchronize()
-    assert _same(ops[0][0].forward(x).cpu(), r.ys[0])
-    assert _same(y1.cpu(), r.ys[1])
-    assert _same(dx0.cpu(), r.dx)
-    for l in range(2):
+    assert _same(dx.cpu(), r.dx)
+    for l in range(L):
         K, M = dims[l], dims[l + 1]
         assert _same(I.w_logical(ops[l][1].tensor, K, M, n[l], True), r.dW[l]), l
         assert ops[l][0].close() == tl.TL_OK

@@ -132,6 +132,39 @@ def test_gemm_dx_accumulate_is_an_fp32_add(tl):
     assert np.array_equal(got.view(np.int32), want.view(np.int32))
 
 
+@pytest.mark.parametrize("T,K,n", SHAPES)
+def test_gemm_dx_bf16_is_accumulate_then_round(tl, T, K, n):
+    """dX rounded to bf16 after adding an fp32 addend (a strided one here) is,
+    bit for bit, the fp32 accumulate into a copy of the addend followed by
+    torch's round to nearest even; with no addend it is the rounded plain
+    product, which also matches the oracle.  Ragged rows and a partial last
+    64-column chunk take the epilogue's bounded loads."""
+    dy = I.make_dy(T, n, seed=T + 5)
+    w = I.make_w_tile(K, n, 1, seed=K + 5)
+    ld_add = K + 8
+    addend = torch.randn(T, ld_add, generator=torch.Generator().manual_seed(T * K)).cuda()
+    dyd, wd = _dev(dy), _dev(w)
+    st = torch.cuda.current_stream().cuda_stream
+    err = _err_word()
+    out = torch.full((T, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tl.tiled_linear_gemm_dx_bf16(T, K, n, dyd.data_ptr(), n, wd.data_ptr(), n, addend.data_ptr(), ld_add,
+                                 out.data_ptr(), K, err.data_ptr(), st)
+    acc = addend[:, :K].contiguous()
+    tl.tiled_linear_gemm_dx(T, K, n, dyd.data_ptr(), n, wd.data_ptr(), n, acc.data_ptr(), K, 1, err.data_ptr(), st)
+    plain_bf16 = torch.full((T, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tl.tiled_linear_gemm_dx_bf16(T, K, n, dyd.data_ptr(), n, wd.data_ptr(), n, None, 0,
+                                 plain_bf16.data_ptr(), K, err.data_ptr(), st)
+    plain = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    tl.tiled_linear_gemm_dx(T, K, n, dyd.data_ptr(), n, wd.data_ptr(), n, plain.data_ptr(), K, 0, err.data_ptr(), st)
+    torch.cuda.synchronize()
+    assert int(err[0].item()) == 0 and int(err[1].item()) == 0
+    assert torch.equal(out.view(torch.int16), acc.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(plain_bf16.view(torch.int16), plain.to(torch.bfloat16).view(torch.int16))
+    dyb, wb = _bits(dy), _bits(w)
+    S = np.abs(bf16_bits_to_f64(dyb)) @ np.abs(bf16_bits_to_f64(wb)).T
+    check("dX bf16", plain_bf16.float().cpu().numpy(), O.backward_dx(dyb, wb), S, n, bf16_out=True)
+
+
 def test_gemm_integer_exact(tl):
     """Entries in {-1, 0, 1}: every partial sum is a small integer, exact in
     fp32 and (|values| <= 256) in bf16, so the GPU must equal the integer
