@@ -96,8 +96,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
     if (lane == 0) ok = wait_bounded(bar, parity, w, code) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) return false;
+    // lane 0 has seen the phase complete, so every lane's first test passes;
+    // the bound only keeps the loop finite
     int mine = 0;
-    for (int n = 0; n < (1 << 20) && !mine; ++n) mine = mbar_try_wait(bar, parity) ? 1 : 0;
+    for (int n = 0; n < (1 << 10) && !mine; ++n) mine = mbar_try_wait(bar, parity) ? 1 : 0;
     if (!mine) atomicOr(w.err, code);
     return __all_sync(0xffffffffu, mine) != 0;
 }
