@@ -500,6 +500,24 @@ def profile_gemms(cfg, reps: int) -> None:
     log(f"[bench] profile-gemms: {reps} x (fwd, dW, dX over {nx} columns) at T={T} K={K} Mi={Mi}")
 
 
+def profile_library_gemm(cfg, reps: int) -> None:
+    """The library's bf16 GEMM (torch.matmul, cuBLAS) on the forward's tile
+    shape, Y_i[T, Mi] = X[T, K] . W_i[K, Mi], `reps` times: the comparison
+    point for the counters of our forward kernel (same inputs, same sizes)."""
+    import torch
+
+    from offload_streamed_gb300 import inputs as I
+    T, K, M, N = cfg["T"], cfg["K"], cfg["M"], cfg["N"]
+    Mi = M // N
+    x = I.make_x(T, K, 0, device="cuda")
+    w1 = I.make_w_tile(K, Mi, 0, 0, device="cuda")
+    y = torch.empty(T, Mi, dtype=torch.bfloat16, device="cuda")
+    for _ in range(reps):
+        torch.matmul(x, w1, out=y)
+    torch.cuda.synchronize()
+    log(f"[bench] profile-library-gemm: {reps} x torch.matmul at T={T} K={K} Mi={Mi}")
+
+
 def run_host_adam(tl, op, x, y, dy, dx, steps: int, dist: Dist, flops_step: float) -> dict:
     """Forward + backward + the Adam step on the host CPU (fp32 master and
     moments, all host threads), the update of each tile overlapping the GPU's
@@ -1206,6 +1224,9 @@ def main():
                          "d = 1..4) and print one JSON line with every point")
     ap.add_argument("--profile-gemms", type=int, default=0, metavar="R",
                     help="only run the three resident GEMMs of one tile R times (for ncu), print nothing")
+    ap.add_argument("--profile-library-gemm", type=int, default=0, metavar="R",
+                    help="only run the library's bf16 GEMM (cuBLAS) on the forward's tile shape R times "
+                         "(for ncu), print nothing")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         log("[bench] note: fewer than 3 warm-up steps")
@@ -1217,6 +1238,9 @@ def main():
         cfg["workload"] += f" (T overridden to {args.T})"
     if args.profile_gemms > 0:
         profile_gemms(cfg, args.profile_gemms)
+        return
+    if args.profile_library_gemm > 0:
+        profile_library_gemm(cfg, args.profile_library_gemm)
         return
     if args.sweep:
         out = run_sweep(args, Dist("nccl"))
