@@ -21,7 +21,6 @@ draw with the same seed, which is harmless because both sides read one copy.
 """
 from __future__ import annotations
 
-import ctypes
 import math
 
 import numpy as np
@@ -111,14 +110,6 @@ def bits(t: torch.Tensor) -> np.ndarray:
     if t.dtype != torch.bfloat16:
         raise TypeError("expected a bf16 tensor")
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-
-
-def host_tensor(ptr: int, numel: int, dtype=torch.bfloat16) -> torch.Tensor:
-    """Wrap ``numel`` elements of host memory at ``ptr`` as a CPU tensor (no
-    copy; the memory stays owned by whoever allocated it)."""
-    itemsize = torch.empty((), dtype=dtype).element_size()
-    buf = (ctypes.c_uint8 * (numel * itemsize)).from_address(ptr)
-    return torch.frombuffer(buf, dtype=torch.uint8).view(dtype)
 
 
 def sample_indices(nrows: int, ncols: int, n: int, seed: int, tensor_id: int,

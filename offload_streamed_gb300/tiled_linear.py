@@ -405,13 +405,22 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def host_tensor(ptr: int, numel: int, dtype=None):
+    """Wrap ``numel`` elements of host memory at ``ptr`` as a CPU tensor (no
+    copy; the memory stays owned by whoever allocated it)."""
+    import torch
+    dtype = dtype or torch.bfloat16
+    itemsize = torch.empty((), dtype=dtype).element_size()
+    buf = (ctypes.c_uint8 * (numel * itemsize)).from_address(ptr)
+    return torch.frombuffer(buf, dtype=torch.uint8).view(dtype)
+
+
 class PinnedBuffer:
     """Page-locked host memory from ``tiled_linear_host_alloc``, viewed as a
     CPU tensor of ``dtype``.  Freed by ``close()`` (or garbage collection)."""
 
     def __init__(self, numel: int, dtype=None):
         import torch
-        from .inputs import host_tensor
         self.dtype = dtype or torch.bfloat16
         self.numel = int(numel)
         itemsize = torch.empty((), dtype=self.dtype).element_size()
