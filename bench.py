@@ -875,7 +875,6 @@ def run_ours(args, cfg, dist: Dist):
     per_step = sorted(marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps))
     ms = dist.max(ms_local)
     st = op.stats()
-    persistent = bool(st.get("persistent", 0))
     launches = args.steps * (st["fwd_launches"] + st["bwd_launches"])
     n_dx = max(st["bwd_launches"] - N, 1)  # dX launches per backward (tile groups)
 
@@ -888,18 +887,13 @@ def run_ours(args, cfg, dist: Dist):
     # --- per-kernel averages over the timed region ---------------------------
     fc, bc = max(st["fwd_timed_calls"], 1), max(st["bwd_timed_calls"], 1)
     op.set_timing(1)
-    if persistent:  # one launch per pass: forward 2TKM, backward 4TKM FLOPs
-        kern = {"fwd_pass (Y = X.W, all tiles)": (st["sum_fwd_gemm_ms"] / fc, 2.0 * T * K * M),
-                "bwd_pass (dW and dX, all tiles)": (st["sum_bwd_gemm_ms"] / bc, 4.0 * T * K * M)}
-    else:
-        flops_launch = 2.0 * T * K * Mi
-        kern = {"fwd_gemm (Y_i = X.W_i)": (st["sum_fwd_gemm_ms"] / (fc * N), flops_launch),
-                "dw_gemm (dW_i = X^T.dY_i)": (st["sum_bwd_dw_gemm_ms"] / (bc * N), flops_launch),
-                "dx_gemm (dX += dY_i.W_i^T over a tile group)": (st["sum_bwd_dx_gemm_ms"] / (bc * n_dx),
-                                                                 2.0 * T * K * M / n_dx)}
-    count = {k: (1 if persistent else N) for k in kern}
-    if not persistent:
-        count["dx_gemm (dX += dY_i.W_i^T over a tile group)"] = n_dx
+    flops_launch = 2.0 * T * K * Mi
+    kern = {"fwd_gemm (Y_i = X.W_i)": (st["sum_fwd_gemm_ms"] / (fc * N), flops_launch),
+            "dw_gemm (dW_i = X^T.dY_i)": (st["sum_bwd_dw_gemm_ms"] / (bc * N), flops_launch),
+            "dx_gemm (dX += dY_i.W_i^T over a tile group)": (st["sum_bwd_dx_gemm_ms"] / (bc * n_dx),
+                                                             2.0 * T * K * M / n_dx)}
+    count = {k: N for k in kern}
+    count["dx_gemm (dX += dY_i.W_i^T over a tile group)"] = n_dx
     dom = max(kern, key=lambda k: kern[k][0] * count[k])
     peak = peaks["bf16_tflops_sustained"]
     dom_ms, dom_flops = kern[dom]
@@ -913,7 +907,7 @@ def run_ours(args, cfg, dist: Dist):
                 "all_kernels_tflops": {k: round(f / (ms / 1e3) / 1e12, 1) for k, (ms, f) in kern.items()
                                        if ms > 0}}
 
-    if not persistent:
+    if True:
         # algorithmic HBM bytes per launch (operands once, outputs once, the
         # dX read-modify-write) and the ncu-measured DRAM bytes, if current
         kind = dom.split(" ")[0]
@@ -936,7 +930,7 @@ def run_ours(args, cfg, dist: Dist):
            "config": {"workload": cfg["workload"], "T": T, "K": K, "M": M, "N": N, "d": d,
                       "host_layout": "tile-major [N][K][M/N]",
                       "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
-                      "launch_mode": "one persistent launch per pass" if persistent else "one launch per tile and GEMM",
+                      "launch_mode": "one launch per tile and GEMM",
                       "kernel_timing": f"CUDA events around every launch of every {TIMING_EVERY}th call "
                                        f"({st['fwd_timed_calls']} of {st['fwd_calls']} steps)",
                       "l2": "inputs larger than L2: W streamed from host every pass, X 128 MiB+, dY 512 MiB+"},
@@ -945,8 +939,6 @@ def run_ours(args, cfg, dist: Dist):
     # where the timed region's time went, from the engine's per-launch and
     # per-copy events summed over every timed call
     gemm_ms = st["sum_fwd_gemm_ms"] + st["sum_bwd_dw_gemm_ms"] + st["sum_bwd_dx_gemm_ms"]
-    if persistent:
-        gemm_ms = st["sum_fwd_gemm_ms"] + st["sum_bwd_gemm_ms"]
     h2d_ms = st["sum_fwd_h2d_ms"] + st["sum_bwd_h2d_ms"]
     out["timed_region"] = {
         "step_ms_median": round(per_step[len(per_step) // 2], 4),
@@ -1016,7 +1008,7 @@ def run_ours(args, cfg, dist: Dist):
     # --- tile reuse (an extension, reported apart from the method's metric) --
     # The backward takes the min(d+1, N) tiles the forward left in the ring
     # instead of fetching them again (tiled_linear_set_tile_reuse).
-    if not args.skip_aux and not persistent:
+    if not args.skip_aux:
         op.set_tile_reuse(True)
         for _ in range(3):
             op.forward(x, y, stream=s)
@@ -1042,17 +1034,17 @@ def run_ours(args, cfg, dist: Dist):
                     "refetches every tile; W unchanged between the two calls)"}
 
     # --- training step with the Adam update on the host CPU (overlapped) -------
-    if not args.skip_aux and not persistent:
+    if not args.skip_aux:
         out["host_adam"] = _extension(lambda: run_host_adam(tl, op, x, y, dy, dx, max(3, min(args.steps, 10)), dist,
                                                             flops_step), dist)
 
     # --- the FFN chain (up- then down-projection) through one prefetcher -------
-    if not args.skip_aux and not persistent and M % K == 0:
+    if not args.skip_aux and M % K == 0:
         out["ffn_chain"] = _extension(lambda: run_ffn_chain(tl, cfg, x, y, dx, args.seed, max(3, min(args.steps, 20)),
                                                             dist), dist)
 
     # --- W and dW one tier further down: files on the box's disk -----------------
-    if not args.skip_aux and not persistent:
+    if not args.skip_aux:
         out["file_tier"] = _extension(lambda: run_file_tier(tl, cfg, w, x, y, dy, dx, 3, dist, flops_step, peaks,
                                                             args.tier_dir), dist)
 

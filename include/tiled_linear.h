@@ -72,11 +72,9 @@ typedef enum { TL_LAYOUT_ROW_MAJOR = 0, TL_LAYOUT_TILE_MAJOR = 1 } tl_layout;
  * tiled_linear_reset_stats was called: fwd_timed_calls / bwd_timed_calls of
  * the fwd_calls / bwd_calls made.  Every call is timed unless
  * tiled_linear_set_timing says otherwise; the first block then describes
- * the last timed call.
- * persistent = 1: each pass ran as ONE persistent launch (fwd_launches =
- * bwd_launches = 1); the backward launch runs both GEMMs, so bwd_gemm_ms is
- * its span and bwd_dw_gemm_ms / bwd_dx_gemm_ms are 0.  persistent = 0: one
- * launch per tile and GEMM; bwd_gemm_ms = bwd_dw_gemm_ms + bwd_dx_gemm_ms. */
+ * the last timed call.  Each call launches one GEMM per tile (and, in the
+ * backward, one dX GEMM per tile group); bwd_gemm_ms = bwd_dw_gemm_ms +
+ * bwd_dx_gemm_ms. */
 typedef struct {
     int32_t n_tiles;
     int32_t depth;            /* d used by the call                           */
@@ -92,17 +90,20 @@ typedef struct {
     double sum_bwd_total_ms, sum_bwd_dw_gemm_ms, sum_bwd_dx_gemm_ms, sum_bwd_h2d_ms, sum_bwd_d2h_ms;
     double sum_bwd_gemm_ms;
     float bwd_gemm_ms;
-    int32_t persistent;
+    int32_t staging_slots;    /* device dW staging slots of the handle       */
     int32_t bwd_reused_tiles; /* tiles the last backward took from the ring
                                  instead of fetching (tiled_linear_set_tile_reuse) */
     int64_t fwd_timed_calls, bwd_timed_calls; /* calls in the sum_* block */
     int32_t timing_every;     /* see tiled_linear_set_timing */
+    float fwd_h2d_max_ms;     /* slowest single tile copy of the last forward */
 } tl_stats;
 
-/* Device workspace bytes needed for (K, M, N, d): (min(d,N-1)+1) weight slots
- * and min(2,N) gradient staging slots of K*(M/N) bf16 each, plus a 64 KiB
- * header (error word, copy-stream flags and per-tile progress counters).  d = -1 (automatic depth) sizes for d = min(N-1, 3).  Returns 0 if
- * the arguments are invalid. */
+/* Device workspace bytes for (K, M, N, d): (min(d,N-1)+1) weight slots and
+ * min(2,N) gradient staging slots of K*(M/N) bf16 each, plus a 4 KiB header
+ * (the kernels' error word and tile counter).  d = -1 (automatic depth): the
+ * most the handle can use, N weight slots and N staging slots; create accepts
+ * any workspace down to 2 weight and min(2,N) staging slots and carves as
+ * many slots as fit.  Returns 0 if the arguments are invalid. */
 size_t tiled_linear_workspace_bytes(int64_t K, int64_t M, int32_t N, int32_t d);
 
 /* Create a handle on `device`.
@@ -111,9 +112,12 @@ size_t tiled_linear_workspace_bytes(int64_t K, int64_t M, int32_t N, int32_t d);
  *            row pitches for the tensor-memory-access engine).
  *  d       : tiles fetched ahead of the one being computed (ring of d+1
  *            slots; d >= N-1 keeps every tile resident).  d = 0 serialises
- *            copy and compute.  d = -1 picks d = ceil(t_fetch / t_layer) from
- *            the first forward call's measured copy and kernel times, bounded
- *            by the workspace.
+ *            copy and compute.  d = -1 (automatic) picks, after the first
+ *            forward call, d = ceil(t_fetch / t_layer) with t_layer that
+ *            call's mean per-tile GEMM time and t_fetch its slowest tile copy
+ *            plus a stall allowance (50 ms by default, see
+ *            tiled_linear_set_stall_allowance), bounded by the weight slots
+ *            the workspace holds; every staging slot that fits is used.
  *  w_host  : pinned host W (read by every call; must not change while a
  *            call is in flight).  dw_host: pinned host dW (overwritten by
  *            every backward call).  Both in tiled_linear_create's layout:
@@ -121,13 +125,8 @@ size_t tiled_linear_workspace_bytes(int64_t K, int64_t M, int32_t N, int32_t d);
  *  workspace_dev, workspace_bytes: device memory, 256-byte aligned, at least
  *            tiled_linear_workspace_bytes(K, M, N, d); owned by the caller,
  *            used until tiled_linear_destroy returns.
- * Execution mode: by default each call launches one GEMM per tile (and per
- * GEMM in the backward), ordered against the copy streams by CUDA events.
- * With the environment variable TILED_LINEAR_PERSISTENT=1 at creation time,
- * and when the shapes allow it (Mi % 256 == 0, d + 1 <= 8, N <= 4096) and
- * the driver's stream memory operations work, each pass instead runs as ONE
- * persistent launch that waits for and releases ring slots through 32-bit
- * flags in the workspace header (tl_stats.persistent reports the mode).
+ * Each call launches one GEMM per tile (and per GEMM in the backward),
+ * ordered against the copy streams by CUDA events.
  * Errors: TL_ERR_INVALID (shapes/pointers), TL_ERR_NOT_PINNED,
  * TL_ERR_WORKSPACE, TL_ERR_CUDA.  On error *out is set to NULL. */
 tl_status tiled_linear_create(tl_handle **out, int64_t K, int64_t M, int32_t N, int32_t d,
@@ -158,8 +157,7 @@ tl_status tiled_linear_create_tilemajor(tl_handle **out, int64_t K, int64_t M, i
  *            as 16 MiB direct-I/O requests spread over them.
  * A tile (K * M/N * 2 bytes) must be a multiple of 4096 bytes.  The other
  * arguments and the workspace are as tiled_linear_create_tilemajor.  The
- * handle runs one launch per tile (never the persistent pass) and takes no
- * host optimizer.  A forward or backward call returns once its last copy is
+ * handle takes no host optimizer.  A forward or backward call returns once its last copy is
  * enqueued, so the calling thread waits for the tile reads (the GPU works on
  * the tiles already there meanwhile), and a backward also waits for free dW
  * slots.  dW is in dw_path only after tiled_linear_file_sync.
@@ -231,9 +229,9 @@ tl_status tiled_linear_get_stats(tl_handle *h, void *tl_stats_out);
  *  kind: TL_TRACE_FWD_GEMM / _DW_GEMM / _DX_GEMM (a dX launch over a group of
  *        tiles is listed under the group's lowest tile), TL_TRACE_H2D (a W
  *        tile into the ring; tiles a backward reused from the ring have none),
- *        TL_TRACE_D2H (a dW tile out), TL_TRACE_PASS (a whole persistent pass).
+ *        TL_TRACE_D2H (a dW tile out).
  *  tile: the tile's index in the handle's order (a chain's operators follow
- *        each other), -1 for a pass.
+ *        each other).
  * Events are listed GEMMs first, in launch order, then copies in fetch order.
  * A copy can start before the call does (a negative start): a weight fetch
  * waits only for its ring slot, not for earlier work on `stream`.
@@ -241,8 +239,7 @@ tl_status tiled_linear_get_stats(tl_handle *h, void *tl_stats_out);
  * there are (0 if no call of that direction was timed).  Waits for that call
  * to finish.  Errors: TL_ERR_INVALID (null handle / count, negative
  * capacity, null out with capacity > 0), TL_ERR_CUDA. */
-enum { TL_TRACE_FWD_GEMM = 0, TL_TRACE_DW_GEMM = 1, TL_TRACE_DX_GEMM = 2, TL_TRACE_H2D = 3, TL_TRACE_D2H = 4,
-       TL_TRACE_PASS = 5 };
+enum { TL_TRACE_FWD_GEMM = 0, TL_TRACE_DW_GEMM = 1, TL_TRACE_DX_GEMM = 2, TL_TRACE_H2D = 3, TL_TRACE_D2H = 4 };
 typedef struct {
     int32_t kind;
     int32_t tile;
@@ -273,9 +270,20 @@ tl_status tiled_linear_set_timing(tl_handle *h, int32_t every);
  * as bwd_reused_tiles, and bwd_h2d_bytes drops by as many tiles.  Results are
  * bit-identical to refetching as long as the host W buffer is not written
  * between the calls; writing it there is undefined.  Default: off.  Errors:
- * TL_ERR_INVALID in the persistent launch mode, TL_ERR_STATE on a failed
- * handle. */
+ * TL_ERR_STATE on a failed handle. */
 tl_status tiled_linear_set_tile_reuse(tl_handle *h, int32_t enable);
+
+/* Stall allowance of the automatic depth (d = -1 at creation), in
+ * milliseconds: the time added to the slowest tile copy of the first forward
+ * call before the depth rule d = ceil(t_fetch / t_layer) is applied
+ * (tm_zero_infinity, "Prefetch depth").  The host link of a shared machine
+ * stalls now and then for tens of milliseconds; a ring sized from mean copy
+ * times stops the GEMMs for the length of such a stall ("Pitfalls": a
+ * mistuned prefetch stalls).  Default 50 ms; 0 applies the rule to the
+ * slowest copy alone.  Takes effect if set before the first forward call;
+ * ignored at a fixed depth.  Errors: TL_ERR_INVALID (ms < 0 or not finite),
+ * TL_ERR_STATE. */
+tl_status tiled_linear_set_stall_allowance(tl_handle *h, double ms);
 
 /* --- the optimizer step on the host ----------------------------------------
  * The Adam update runs on the CPU, beside the DRAM holding its state: it is
@@ -326,7 +334,7 @@ tl_status tiled_linear_adam_update(const tl_adam_config *cfg, int64_t step, int6
  * forward / backward may therefore block the calling thread.  Results are
  * bit-identical to calling tiled_linear_adam_update tile by tile after the
  * backward completes.  Host waits give up after 600 s with TL_ERR_TIMEOUT.
- * Errors: TL_ERR_INVALID (arguments, persistent mode, a handle whose W and
+ * Errors: TL_ERR_INVALID (arguments, a handle whose W and
  * dW are in files, accumulate without an accumulator), TL_ERR_STATE (no backward since the last optimizer call, or
  * an optimizer already attached), TL_ERR_CUDA, TL_ERR_TIMEOUT. */
 typedef struct tl_optimizer tl_optimizer;

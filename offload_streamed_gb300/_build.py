@@ -1,7 +1,7 @@
 """Build the CUDA library in-tree: ``offload_streamed_gb300/_lib/libtiled_linear.so``.
 
-The translation units (GEMM kernels, engine / C ABI, allocation-free
-forward) are compiled in parallel by nvcc for sm_103a only, then linked against the shared CUDA
+The translation units (GEMM kernels, the engine's ring, stats, hooks and C
+ABI, the allocation-free forward, the host optimizer and the file tier) are compiled in parallel by nvcc for sm_103a only, then linked against the shared CUDA
 runtime (the same ``libcudart.so.13`` PyTorch loads, so streams created by
 either side are one runtime's streams).  The build is skipped when the shared
 library is newer than every source and header.
@@ -29,8 +29,8 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompil
 # Extra flags of single units: the host optimizer's row loop vectorizes its
 # square roots only without errno semantics.
 UNIT_FLAGS = {"tl_adam.cpp": ["-Xcompiler", "-fno-math-errno"]}
-UNITS = ["tl_gemm.cu", "tl_pass.cu", "tl_engine.cu", "tl_static.cu", "tl_adam.cpp", "tl_filetier.cpp",
-         "tl_optimizer.cpp"]
+UNITS = ["tl_gemm.cu", "tl_static.cu", "tl_ring.cpp", "tl_stats.cpp", "tl_hooks.cpp", "tl_abi.cpp", "tl_adam.cpp",
+         "tl_filetier.cpp", "tl_optimizer.cpp"]
 
 
 def nvcc() -> str:

@@ -411,11 +411,6 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-bool make_tensor_map(void* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer,
-                     bool f32, std::string* why) {
-    return make_map(static_cast<CUtensorMap*>(map), base, inner, outer, ld, box_outer, why, f32);
-}
-
 // Choose the tile order that moves the fewest operand bytes from DRAM: keep
 // a group of one operand's blocks (at most kL2Budget bytes) resident in L2
 // and stream the other operand once per group.  The budget is a quarter of

@@ -60,59 +60,10 @@ struct GemmDesc {
 // Returns an empty string if `g` can be launched, else the reason.
 std::string gemm_check(const GemmDesc& g);
 
-// Enqueue one GEMM on `stream`.  num_sms = persistent grid bound.
+// Enqueue one GEMM on `stream`.  num_sms bounds the persistent grid.
 cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std::string* why);
 
-// ---- persistent streamed pass ------------------------------------------------
-// One launch runs a whole forward or backward pass over the N weight tiles,
-// synchronised with the copy streams through 32-bit sequence flags in device
-// memory (written by stream memory operations on the copy streams and by the
-// kernel; compared wrap-safely as (int32)(value - target) >= 0):
-//   flags[kFlagReady + s]   = f + 1 once fetch f has landed in ring slot s
-//   flags[kFlagFreed + s]   = f + 1 once every job reading fetch f is done
-//   flags[kFlagDwReady + g] = j + 1 once staging slot g holds complete dW of stage j
-//   flags[kFlagDrained + g] = j + 1 once stage j has been copied back to the host
-constexpr int kMaxPassSlots = 8;
-constexpr int kMaxPassStages = 2;
-constexpr int kMaxPassTiles = 4096;
-constexpr int kFlagReady = 0, kFlagFreed = 8, kFlagDwReady = 16, kFlagDrained = 18, kNumFlags = 20;
-
-struct PassDesc {
-    bool backward = false;
-    int64_t T = 0, K = 0, Mi = 0;
-    int32_t N = 0;
-    const void* x = nullptr;   // [T, K] bf16
-    const void* dy = nullptr;  // [T, N*Mi] bf16 (backward)
-    void* y = nullptr;         // [T, N*Mi] bf16 (forward)
-    float* dx = nullptr;       // [T, K] fp32 (backward)
-    void* slots[kMaxPassSlots] = {};
-    int32_t nslots = 0;
-    void* stages[kMaxPassStages] = {};
-    int32_t nstage = 0;
-    uint32_t fetch_base = 0;   // fetch sequence number of the pass's first tile
-    uint32_t stage_base = 0;   // staging sequence number of the pass's first dW tile
-    int32_t dx_group = 1;      // backward: tiles per dX accumulation group (<= nslots)
-    uint32_t* flags = nullptr;
-    uint32_t* done = nullptr;     // [N] per pass position, zeroed before the launch
-    uint32_t* dwdone = nullptr;   // [N]
-    uint32_t* dxdone = nullptr;   // [N]
-    int32_t* err = nullptr;
-    uint64_t timeout_ns = 2000000000ull;
-    uint64_t flag_timeout_ns = 10000000000ull;
-};
-
-// Empty if a persistent pass can run with these shapes (tile width a multiple
-// of 256, at most kMaxPassSlots ring slots, ...), else the reason.
-std::string pass_check(const PassDesc& d, int num_sms);
-cudaError_t pass_launch(const PassDesc& d, int num_sms, cudaStream_t stream, std::string* why);
-// Load the pass kernels now (lazy module loading may otherwise load them at
-// their first launch, which can wait for the device to drain -- unsafe once
-// copy streams are waiting on flags that only the pass kernel will write).
-cudaError_t pass_preload();
-
 // Shared host helpers (defined in tl_gemm.cu).
-bool make_tensor_map(void* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer,
-                     bool f32, std::string* why);
 void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int32_t* raster, int32_t* group);
 bool cta_pair_enabled();
 
@@ -128,7 +79,6 @@ enum : int32_t {
     kErrMmaWaitTmem = 4,
     kErrEpilogueWait = 8,
     kErrDrainWait = 16,
-    kErrFlagWait = 32,  // a persistent pass gave up waiting for a copy-stream flag
     kErrTileQueueWait = 64,  // a role gave up waiting for the next tile of the dynamic schedule
 };
 

@@ -1,7 +1,6 @@
-// tl_kernel_common.cuh -- device building blocks shared by the per-tile GEMM
-// kernel (tl_gemm.cu) and the persistent streamed-pass kernel (tl_pass.cu):
-// tile geometry, bounded waits, tile order, shared-memory operand
-// descriptors, the two epilogue paths, and acquire / release flag helpers.
+// tl_kernel_common.cuh -- device building blocks of the GEMM kernel
+// (tl_gemm.cu): tile geometry, bounded waits, tile order, shared-memory
+// operand descriptors and the epilogue paths.
 #pragma once
 #include "tl_gemm.h"
 #include "tl_ptx.cuh"
@@ -263,40 +262,6 @@ __device__ __forceinline__ void epi_f32_tma(const CUtensorMap* map, uint32_t t_r
             bulk_commit_group();
         }
         buf ^= 1u;
-    }
-}
-
-// ---- flags in global memory ----------------------------------------------------
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Order this thread's earlier generic-proxy accesses (e.g. a flag it read)
-// before its later async-proxy (TMA) accesses of global memory.
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Wait (bounded by limit_ns) until the 32-bit sequence value at p has reached
-// `target` (wrap-safe: (int32)(value - target) >= 0).  One thread.
-__device__ __noinline__ inline bool poll_geq(const uint32_t* p, uint32_t target, const WaitCtx& w, int32_t code,
-                                             uint64_t limit_ns) {
-    if (int32_t(ld_acquire_u32(p) - target) >= 0) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t n = 1;; ++n) {
-        __nanosleep(200);
-        if (int32_t(ld_acquire_u32(p) - target) >= 0) return true;
-        if ((n & 63u) == 0) {
-            if (*reinterpret_cast<volatile int32_t*>(w.err) != 0) return false;
-            if (global_timer_ns() - t0 > limit_ns) {
-                atomicOr(w.err, code);
-                return false;
-            }
-        }
     }
 }
 

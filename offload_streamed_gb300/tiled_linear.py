@@ -44,9 +44,10 @@ class tl_stats(ctypes.Structure):
         ("sum_fwd_h2d_ms", ctypes.c_double), ("sum_bwd_total_ms", ctypes.c_double),
         ("sum_bwd_dw_gemm_ms", ctypes.c_double), ("sum_bwd_dx_gemm_ms", ctypes.c_double),
         ("sum_bwd_h2d_ms", ctypes.c_double), ("sum_bwd_d2h_ms", ctypes.c_double),
-        ("sum_bwd_gemm_ms", ctypes.c_double), ("bwd_gemm_ms", ctypes.c_float), ("persistent", ctypes.c_int32),
+        ("sum_bwd_gemm_ms", ctypes.c_double), ("bwd_gemm_ms", ctypes.c_float), ("staging_slots", ctypes.c_int32),
         ("bwd_reused_tiles", ctypes.c_int32),
         ("fwd_timed_calls", ctypes.c_int64), ("bwd_timed_calls", ctypes.c_int64), ("timing_every", ctypes.c_int32),
+        ("fwd_h2d_max_ms", ctypes.c_float),
     ]
 
     def as_dict(self) -> dict:
@@ -63,8 +64,8 @@ class tl_file_stats(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
-TL_TRACE_FWD_GEMM, TL_TRACE_DW_GEMM, TL_TRACE_DX_GEMM, TL_TRACE_H2D, TL_TRACE_D2H, TL_TRACE_PASS = range(6)
-TRACE_KINDS = {0: "fwd_gemm", 1: "dw_gemm", 2: "dx_gemm", 3: "h2d", 4: "d2h", 5: "pass"}
+TL_TRACE_FWD_GEMM, TL_TRACE_DW_GEMM, TL_TRACE_DX_GEMM, TL_TRACE_H2D, TL_TRACE_D2H = range(5)
+TRACE_KINDS = {0: "fwd_gemm", 1: "dw_gemm", 2: "dx_gemm", 3: "h2d", 4: "d2h"}
 
 
 class tl_trace_event(ctypes.Structure):
@@ -129,6 +130,8 @@ def load():
         L.tiled_linear_set_tile_reuse.restype = st
         L.tiled_linear_set_timing.argtypes = [vp, i32]
         L.tiled_linear_set_timing.restype = st
+        L.tiled_linear_set_stall_allowance.argtypes = [vp, ctypes.c_double]
+        L.tiled_linear_set_stall_allowance.restype = st
         L.tiled_linear_adam_update.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, vp]
         L.tiled_linear_adam_update.restype = st
         L.tiled_linear_optimizer_create.argtypes = [ctypes.POINTER(vp), vp, vp, vp, vp, vp, vp]
@@ -264,6 +267,10 @@ def tiled_linear_set_timing(h: int, every: int) -> None:
 
 def tiled_linear_set_tile_reuse(h: int, enable: bool) -> None:
     _check(load().tiled_linear_set_tile_reuse(h, 1 if enable else 0), "tiled_linear_set_tile_reuse", h)
+
+
+def tiled_linear_set_stall_allowance(h: int, ms: float) -> None:
+    _check(load().tiled_linear_set_stall_allowance(h, float(ms)), "tiled_linear_set_stall_allowance", h)
 
 
 def _i64s(v):
@@ -447,10 +454,14 @@ class TiledLinear:
 
     w_host / dw_host: pinned host buffers (``PinnedBuffer`` or a pinned CPU
     tensor) of K*M bf16 each, tile-major [N][K][M/N] when ``tile_major`` else
-    row-major [K][M].  The workspace is a device uint8 tensor owned here."""
+    row-major [K][M].  The workspace is a device uint8 tensor owned here.
+
+    d = -1 (automatic depth): the workspace holds as many ring and staging
+    slots as ``auto_workspace_bytes`` allows (default: half of the device's
+    free memory), at most N of each."""
 
     def __init__(self, K: int, M: int, N: int, d: int, w_host, dw_host, *, tile_major: bool = True,
-                 device=None):
+                 device=None, auto_workspace_bytes: int | None = None):
         import torch
         self.K, self.M, self.N, self.d = int(K), int(M), int(N), int(d)
         self.Mi = self.M // self.N
@@ -461,6 +472,12 @@ class TiledLinear:
         if wb == 0:
             raise TiledLinearError(TL_ERR_INVALID, "tiled_linear_workspace_bytes",
                                    f"invalid shape K={K} M={M} N={N} d={d}")
+        if self.d < 0:
+            least = tiled_linear_workspace_bytes(self.K, self.M, self.N, min(1, self.N - 1))
+            budget = auto_workspace_bytes
+            if budget is None:
+                budget = torch.cuda.mem_get_info(self.device)[0] // 2
+            wb = max(least, min(wb, int(budget)))
         self.workspace = torch.empty(wb, dtype=torch.uint8, device=self.device)
         self._w, self._dw = w_host, dw_host
         wp = w_host.ptr if isinstance(w_host, PinnedBuffer) else w_host.data_ptr()
@@ -504,6 +521,10 @@ class TiledLinear:
     def set_timing(self, every: int) -> None:
         """Record per-launch / per-copy timing events on every `every`-th call."""
         tiled_linear_set_timing(self.handle, every)
+
+    def set_stall_allowance(self, ms: float) -> None:
+        """Automatic depth: host-link stall (ms) the ring is sized to ride out."""
+        tiled_linear_set_stall_allowance(self.handle, ms)
 
     def close(self) -> int:
         st = TL_OK

@@ -11,7 +11,7 @@ from oracle import closed_forms as CF
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER_FILE = os.path.join(ROOT, "include", "tiled_linear.h")
-HEADER = 65536  # workspace control block: error word, pass flags and counters
+HEADER = 4096  # workspace header: the kernels' error word and tile counter
 
 
 @pytest.fixture(scope="module")
@@ -64,9 +64,24 @@ def test_workspace_bytes_matches_closed_form(tl, K, M, N, d):
 
 
 def test_workspace_bytes_auto_depth(tl):
+    """Automatic depth sizes for the most a handle can use: N ring slots (every
+    tile resident, d = N - 1) and N staging slots."""
     tile = CF.tile_bytes(1024, 4096, 4)
-    assert tl.tiled_linear_workspace_bytes(1024, 4096, 4, -1) == HEADER + (4 + 2) * tile
-    assert tl.tiled_linear_workspace_bytes(1024, 4096 * 4, 16, -1) == HEADER + (4 + 2) * tile
+    assert tl.tiled_linear_workspace_bytes(1024, 4096, 4, -1) == HEADER + (4 + 4) * tile
+    assert tl.tiled_linear_workspace_bytes(1024, 4096 * 4, 16, -1) == HEADER + (16 + 16) * tile
+    assert tl.tiled_linear_workspace_bytes(1024, 4096, 1, -1) == HEADER + (1 + 1) * 4 * tile
+
+
+def test_auto_depth_accepts_a_smaller_workspace(tl):
+    """Create with d = -1 refuses less than two ring slots and min(2, N)
+    staging slots (the d = 1 workspace), and accepts that much."""
+    K, M, N = 64, 64 * 8, 8
+    least = tl.tiled_linear_workspace_bytes(K, M, N, 1)
+    assert least < tl.tiled_linear_workspace_bytes(K, M, N, -1)
+    with pytest.raises(tl.TiledLinearError) as ei:
+        tl.tiled_linear_create(K, M, N, -1, 16, 16, 256, least - 1, 0)
+    assert ei.value.status == tl.TL_ERR_WORKSPACE
+    assert str(least) in tl.tiled_linear_last_error(None)
 
 
 @pytest.mark.parametrize("K,M,N,d", [(0, 64, 1, 0), (12, 64, 1, 0), (64, 65, 1, 0), (64, 64, 3, 0),
@@ -129,6 +144,29 @@ def test_trace_argument_checks(tl):
 
 def test_null_handle_tile_reuse(tl):
     assert tl.load().tiled_linear_set_tile_reuse(None, 1) == tl.TL_ERR_STATE
+    assert tl.load().tiled_linear_set_stall_allowance(None, 1.0) == tl.TL_ERR_STATE
+
+
+def test_forward_static_argument_checks(tl):
+    """The allocation-free forward refuses bad shapes, oversized tiles and a
+    missing status word before any CUDA call, and keeps the reason where
+    tiled_linear_last_error(NULL) finds it."""
+    lib = tl.load()
+    st = ctypes.c_void_p(16)
+    assert lib.tiled_linear_forward_static(16, 12, 64, 1, None, None, None, st, None) == tl.TL_ERR_INVALID
+    assert "K % 8" in tl.tiled_linear_last_error(None)
+    assert lib.tiled_linear_forward_static(1 << 30, 64, 64, 1, None, None, None, st, None) == tl.TL_ERR_INVALID
+    assert lib.tiled_linear_forward_static(16, 1 << 30, 64, 1, None, None, None, st, None) == tl.TL_ERR_INVALID
+    # one tile of 8192 x 4096 bf16 = 64 MiB > the 32 MiB static slot
+    assert lib.tiled_linear_forward_static(16, 8192, 8192, 2, None, None, None, st, None) == tl.TL_ERR_WORKSPACE
+    assert "static slot" in tl.tiled_linear_last_error(None)
+    # K * (M/N) * 2 would overflow 64 bits if multiplied first
+    assert lib.tiled_linear_forward_static(16, (1 << 30) - 8, (1 << 30) - 8, 1, None, None, None, st, None) \
+        == tl.TL_ERR_WORKSPACE
+    # the largest tile that fits: 2048 x 8184 bf16 = 32 MiB - 32,768 bytes
+    assert lib.tiled_linear_forward_static(16, 2048, 8184, 1, 16, 16, 16, None, None) == tl.TL_ERR_INVALID
+    assert "status_host" in tl.tiled_linear_last_error(None)
+    assert lib.tiled_linear_forward_static(16, 2048, 8192, 1, 16, 16, 16, st, None) == tl.TL_ERR_WORKSPACE
 
 
 @pytest.mark.parametrize("struct", ["tl_stats", "tl_file_stats", "tl_adam_config", "tl_trace_event"])

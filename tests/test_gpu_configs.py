@@ -118,5 +118,6 @@ def test_64k_hidden_ffn(tl):
 @pytest.mark.parametrize("T,d", [(512, 4), (65536, 1)])
 def test_ait_sweep_points(tl, T, d):
     """K = 16384, M = 65536, N = 16 tiles of 4096: the sweep's smallest and
-    largest token counts."""
-    _run_config(tl, T, 16384, 65536, 16, depths=(d,), untiled=(T <= 8192))
+    largest token counts.  At T = 65536 the untiled check holds X (2 GiB), W
+    (2 GiB) and two Y of 8 GiB on the device besides the run's dY and dX."""
+    _run_config(tl, T, 16384, 65536, 16, depths=(d,))

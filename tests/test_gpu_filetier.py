@@ -71,7 +71,7 @@ def test_file_tier_equals_the_host_memory_path(tl, tmp_path, K, M, N, d, slots, 
     assert fs["write_bytes"] == 2 * N * tb
     assert fs["host_slots"] == slots and fs["io_threads"] == io
     st = op.stats()
-    assert st["persistent"] == 0 and st["fwd_h2d_bytes"] == N * tb
+    assert st["staging_slots"] == min(2, N) and st["fwd_h2d_bytes"] == N * tb
     for o in (op, ref):
         assert o.close() == tl.TL_OK
     w.close()

@@ -1,5 +1,7 @@
 """The streamed tiled linear operator end to end through the C ABI (host W in
 pinned memory, depth-d ring, copy streams) against the CPU oracle."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -23,21 +25,11 @@ class Run:
     pass
 
 
-def make_op(tl, K, M, N, d, w, dw, tile_major=True, persistent=True):
-    """Create a handle; persistent=False forces one launch per tile and GEMM."""
-    import os
-    old = os.environ.get("TILED_LINEAR_PERSISTENT")
-    os.environ["TILED_LINEAR_PERSISTENT"] = "1" if persistent else "0"
-    try:
-        return tl.TiledLinear(K, M, N, d, w, dw, tile_major=tile_major)
-    finally:
-        if old is None:
-            del os.environ["TILED_LINEAR_PERSISTENT"]
-        else:
-            os.environ["TILED_LINEAR_PERSISTENT"] = old
+def make_op(tl, K, M, N, d, w, dw, tile_major=True):
+    return tl.TiledLinear(K, M, N, d, w, dw, tile_major=tile_major)
 
 
-def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, stream=None, persistent=True,
+def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, stream=None,
            reuse=False, extra_backward=False):
     r = Run()
     w = tl.PinnedBuffer(K * M)
@@ -46,7 +38,7 @@ def run_op(tl, T, K, M, N, d, tile_major=True, seed=0, kind="normal", calls=1, s
     dw.tensor.view(torch.int16).fill_(0x7FC0)  # NaN: catches tiles never written
     x = I.make_x(T, K, seed, kind=kind)
     dy = I.make_dy(T, M, seed, kind=kind)
-    op = make_op(tl, K, M, N, d, w, dw, tile_major=tile_major, persistent=persistent)
+    op = make_op(tl, K, M, N, d, w, dw, tile_major=tile_major)
     if reuse:
         op.set_tile_reuse(True)
     xd, dyd = x.cuda(), dy.cuda()
@@ -82,21 +74,17 @@ def oracle_check(r, T, K, M):
     check("dW", r.dw.float().numpy(), dW, xa.T @ dya, T, True)
 
 
-@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "per_tile"])
 @pytest.mark.parametrize("tile_major", [True, False], ids=["tilemajor", "rowmajor"])
-def test_tiny_config_full_parity(tl, tile_major, persistent):
+def test_tiny_config_full_parity(tl, tile_major):
     """X [256,1024], W [1024,4096] in N=4 tiles, dY [256,4096], d=1."""
     T, K, M, N, d = 256, 1024, 4096, 4, 1
-    r = run_op(tl, T, K, M, N, d, tile_major=tile_major, persistent=persistent)
+    r = run_op(tl, T, K, M, N, d, tile_major=tile_major)
     oracle_check(r, T, K, M)
     st = r.stats
-    assert st["persistent"] == int(persistent)
-    if persistent:
-        assert st["fwd_launches"] == 1 and st["bwd_launches"] == 1
-    else:
-        # one dW launch per tile, one dX launch per group of tiles
-        g = dx_group(d, N, M // N)
-        assert st["fwd_launches"] == N and st["bwd_launches"] == N + (N + g - 1) // g
+    # one dW launch per tile, one dX launch per group of tiles
+    g = dx_group(d, N, M // N)
+    assert st["fwd_launches"] == N and st["bwd_launches"] == N + (N + g - 1) // g
+    assert st["staging_slots"] == 2
     assert st["fwd_h2d_bytes"] == K * M * 2 and st["bwd_h2d_bytes"] == K * M * 2
     assert st["bwd_d2h_bytes"] == K * M * 2
     assert st["depth"] == d
@@ -132,31 +120,29 @@ def dx_group(depth, N, Mi):
 
 
 def test_schedule_does_not_change_results(tl):
-    """Depth, host layout, repeated calls and the launch mode change only the
-    schedule: Y and dW are bit-identical for every schedule; dX (an fp32 sum
-    whose grouping is part of the schedule) is bit-identical among schedules
-    with the same dX grouping and matches the oracle for every one."""
+    """Depth, host layout and repeated calls change only the schedule: Y and dW
+    are bit-identical for every schedule; dX (an fp32 sum whose grouping is
+    part of the schedule) is bit-identical among schedules with the same dX
+    grouping and matches the oracle for every one."""
     T, K, M, N = 200, 264, 2048, 8
-    base = {g: run_op(tl, T, K, M, N, g - 1, tile_major=True, seed=7, persistent=False) for g in (1, 2, 3, 4)}
+    base = {g: run_op(tl, T, K, M, N, g - 1, tile_major=True, seed=7) for g in (1, 2, 3, 4)}
     for g, r in base.items():
         assert dx_group(r.stats["depth"], N, M // N) == g
         oracle_check(r, T, K, M)
-    for d, tm, calls, pers in [(0, True, 1, True), (2, True, 1, True), (3, False, 1, True), (7, True, 2, True),
-                               (12, False, 1, True), (-1, True, 3, True), (1, True, 1, False),
-                               (0, False, 2, False), (5, True, 1, False), (-1, True, 2, False)]:
-        r = run_op(tl, T, K, M, N, d, tile_major=tm, seed=7, calls=calls, persistent=pers)
+    for d, tm, calls in [(0, True, 1), (2, True, 1), (3, False, 1), (7, True, 2), (12, False, 1), (-1, True, 3),
+                         (1, True, 1), (0, False, 2), (5, True, 1), (-1, False, 2)]:
+        r = run_op(tl, T, K, M, N, d, tile_major=tm, seed=7, calls=calls)
         ref = base[dx_group(r.stats["depth"], N, M // N)]
-        assert _same(r.y, ref.y), (d, tm, pers)
-        assert _same(r.dw, ref.dw), (d, tm, pers)
-        assert _same(r.dx, ref.dx), (d, tm, pers)
+        assert _same(r.y, ref.y), (d, tm)
+        assert _same(r.dw, ref.dw), (d, tm)
+        assert _same(r.dx, ref.dx), (d, tm)
 
 
-@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "per_tile"])
-def test_dx_grouping_matches_oracle_for_odd_tile_counts(tl, persistent):
+def test_dx_grouping_matches_oracle_for_odd_tile_counts(tl):
     """N odd: the last dX group holds a single tile."""
     T, K, M = 160, 512, 5 * 512
     for d in (1, 2, 4):
-        r = run_op(tl, T, K, M, 5, d, seed=13, persistent=persistent)
+        r = run_op(tl, T, K, M, 5, d, seed=13)
         oracle_check(r, T, K, M)
 
 
@@ -208,7 +194,6 @@ def test_ragged_tile_width_runs_per_tile(tl, K, M, N):
     a width of 320 (five 64-deep K-blocks) still pairs the dX tiles."""
     T = 150
     r = run_op(tl, T, K, M, N, 1, seed=K)
-    assert r.stats["persistent"] == 0
     oracle_check(r, T, K, M)
 
 
@@ -239,10 +224,9 @@ def test_side_stream_and_default_stream(tl):
     assert _same(a.y, b.y) and _same(a.dx, b.dx) and _same(a.dw, b.dw)
 
 
-@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "per_tile"])
-def test_stats_are_consistent(tl, persistent):
+def test_stats_are_consistent(tl):
     T, K, M, N = 512, 1024, 8192, 8
-    r = run_op(tl, T, K, M, N, 2, seed=1, calls=2, persistent=persistent)
+    r = run_op(tl, T, K, M, N, 2, seed=1, calls=2)
     st = r.stats
     assert st["fwd_valid"] == 1 and st["bwd_valid"] == 1
     assert st["n_tiles"] == N and st["depth"] == 2
@@ -250,19 +234,63 @@ def test_stats_are_consistent(tl, persistent):
     for k in ("fwd_total_ms", "fwd_gemm_ms", "fwd_h2d_ms", "bwd_total_ms", "bwd_gemm_ms", "bwd_h2d_ms",
               "bwd_d2h_ms"):
         assert st[k] > 0, k
-    if not persistent:
-        assert st["bwd_launches"] == N + (N + 2) // 3  # d = 2: groups of three
-        assert st["bwd_dw_gemm_ms"] > 0 and st["bwd_dx_gemm_ms"] > 0
-        assert abs(st["bwd_dw_gemm_ms"] + st["bwd_dx_gemm_ms"] - st["bwd_gemm_ms"]) < 1e-3
+    assert st["bwd_launches"] == N + (N + 2) // 3  # d = 2: groups of three
+    assert st["bwd_dw_gemm_ms"] > 0 and st["bwd_dx_gemm_ms"] > 0
+    assert abs(st["bwd_dw_gemm_ms"] + st["bwd_dx_gemm_ms"] - st["bwd_gemm_ms"]) < 1e-3
+    assert 0 < st["fwd_h2d_max_ms"] <= st["fwd_h2d_ms"] + 1e-3
     assert st["fwd_gemm_ms"] <= st["fwd_total_ms"] + 1e-3
     assert st["bwd_gemm_ms"] <= st["bwd_total_ms"] + 1e-3
 
 
 def test_auto_depth_picks_within_ring(tl):
+    """With room for every tile, the default stall allowance (50 ms, far more
+    than these tiles' GEMMs take) keeps every tile in the ring, and every
+    staging slot is used; results match the oracle."""
     T, K, M, N = 256, 1024, 8192, 8
     r = run_op(tl, T, K, M, N, -1, seed=2, calls=2)
-    assert 1 <= r.stats["depth"] <= 4
+    assert r.stats["depth"] == N - 1 and r.stats["staging_slots"] == N
     oracle_check(r, T, K, M)
+
+
+def _auto_op(tl, K, M, N, seed, **kw):
+    w = tl.PinnedBuffer(K * M)
+    dw = tl.PinnedBuffer(K * M)
+    I.fill_w_host(w.tensor, K, M, N, True, seed)
+    return tl.TiledLinear(K, M, N, -1, w, dw, **kw), w, dw
+
+
+def test_auto_depth_rule_and_workspace_bound(tl):
+    """Without a stall allowance the rule d = ceil(t_fetch / t_layer) is
+    applied to the first forward's slowest copy and mean GEMM time (recorded
+    in the stats); the smallest workspace allowed gives d = 1 and two staging
+    slots."""
+    T, K, M, N = 512, 2048, 8 * 1024, 8
+    x = I.make_x(T, K, 4).cuda()
+    op, w, dw = _auto_op(tl, K, M, N, 4)
+    op.set_stall_allowance(0.0)
+    y1 = op.forward(x)
+    st1 = op.stats()
+    y2 = op.forward(x)  # the depth is chosen before this call
+    torch.cuda.synchronize()
+    st = op.stats()
+    t_layer = st1["fwd_gemm_ms"] / N
+    want = max(1, min(N - 1, math.ceil(st1["fwd_h2d_max_ms"] / t_layer)))
+    assert st["depth"] == want, (st1, st)
+    assert _same(y1.cpu(), y2.cpu())
+    with pytest.raises(tl.TiledLinearError):
+        op.set_stall_allowance(-1.0)
+    op.close()
+    least = tl.tiled_linear_workspace_bytes(K, M, N, 1)
+    small, w2, dw2 = _auto_op(tl, K, M, N, 4, auto_workspace_bytes=least)
+    y3 = small.forward(x)
+    small.forward(x)
+    torch.cuda.synchronize()
+    st = small.stats()
+    assert st["depth"] == 1 and st["staging_slots"] == 2
+    assert _same(y3.cpu(), y1.cpu())
+    small.close()
+    for b in (w, dw, w2, dw2):
+        b.close()
 
 
 def test_not_pinned_is_rejected(tl):
@@ -295,8 +323,8 @@ def test_tile_reuse_is_bit_identical_and_skips_fetches(tl, N, d, calls):
     the ring instead of fetching them again: same bits, fewer H2D bytes."""
     T, K, Mi = 192, 512, 512
     M = N * Mi
-    ref = run_op(tl, T, K, M, N, d, seed=21, calls=calls, persistent=False)
-    r = run_op(tl, T, K, M, N, d, seed=21, calls=calls, persistent=False, reuse=True)
+    ref = run_op(tl, T, K, M, N, d, seed=21, calls=calls)
+    r = run_op(tl, T, K, M, N, d, seed=21, calls=calls, reuse=True)
     assert _same(r.y, ref.y) and _same(r.dw, ref.dw) and _same(r.dx, ref.dx)
     oracle_check(r, T, K, M)
     want = min(r.stats["depth"] + 1, N)
@@ -309,35 +337,21 @@ def test_tile_reuse_after_a_backward_refetches(tl):
     """After a backward the ring holds the first tiles, not the ones a
     backward starts with: the next backward fetches everything again."""
     T, K, M, N = 160, 512, 4 * 512, 4
-    ref = run_op(tl, T, K, M, N, 1, seed=5, calls=2, persistent=False, extra_backward=True)
-    r = run_op(tl, T, K, M, N, 1, seed=5, calls=2, persistent=False, reuse=True, extra_backward=True)
+    ref = run_op(tl, T, K, M, N, 1, seed=5, calls=2, extra_backward=True)
+    r = run_op(tl, T, K, M, N, 1, seed=5, calls=2, reuse=True, extra_backward=True)
     assert _same(r.y, ref.y) and _same(r.dw, ref.dw) and _same(r.dx, ref.dx)
     assert r.stats["bwd_reused_tiles"] == 0
     oracle_check(r, T, K, M)
-
-
-def test_tile_reuse_needs_per_tile_mode(tl):
-    K, M, N = 512, 1024, 2
-    w, dw = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
-    op = make_op(tl, K, M, N, 1, w, dw, persistent=True)
-    assert op.stats()["persistent"] == 1
-    with pytest.raises(tl.TiledLinearError) as ei:
-        op.set_tile_reuse(True)
-    assert ei.value.status == tl.TL_ERR_INVALID
-    op.set_tile_reuse(False)
-    assert op.close() == tl.TL_OK
-    w.close()
-    dw.close()
 
 
 def test_sampled_timing_counts_and_results(tl):
     """Timing every third call: all calls counted, three of seven timed, the
     results unchanged."""
     T, K, M, N = 128, 512, 2048, 4
-    ref = run_op(tl, T, K, M, N, 1, seed=3, calls=1, persistent=False)
+    ref = run_op(tl, T, K, M, N, 1, seed=3, calls=1)
     w, dw = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
     I.fill_w_host(w.tensor, K, M, N, True, 3)
-    op = make_op(tl, K, M, N, 1, w, dw, persistent=False)
+    op = make_op(tl, K, M, N, 1, w, dw)
     op.set_timing(3)
     xd, dyd = ref.x.cuda(), ref.dy.cuda()
     for _ in range(7):

@@ -21,19 +21,10 @@ def tl():
     return tiled_linear
 
 
-def _op(tl, K, M, N, d, persistent=False):
-    import os
-    old = os.environ.get("TILED_LINEAR_PERSISTENT")
-    os.environ["TILED_LINEAR_PERSISTENT"] = "1" if persistent else "0"
-    try:
-        w, dw = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
-        I.fill_w_host(w.tensor, K, M, N, True, 1)
-        return tl.TiledLinear(K, M, N, d, w, dw, tile_major=True), (w, dw)
-    finally:
-        if old is None:
-            del os.environ["TILED_LINEAR_PERSISTENT"]
-        else:
-            os.environ["TILED_LINEAR_PERSISTENT"] = old
+def _op(tl, K, M, N, d):
+    w, dw = tl.PinnedBuffer(K * M), tl.PinnedBuffer(K * M)
+    I.fill_w_host(w.tensor, K, M, N, True, 1)
+    return tl.TiledLinear(K, M, N, d, w, dw, tile_major=True), (w, dw)
 
 
 def _by(trace, kind):
@@ -96,22 +87,6 @@ def test_reused_tiles_have_no_copy(tl):
     _steps(op, T, K, M)
     bh = _by(op.trace(True), "h2d")
     assert sorted(bh) == list(range(N - (d + 1)))  # the forward's last d+1 tiles stayed in the ring
-    assert op.close() == tl.TL_OK
-    for b in bufs:
-        b.close()
-
-
-def test_persistent_pass_is_one_span(tl):
-    T, K, M, N, d = 256, 512, 4096, 4, 1
-    op, bufs = _op(tl, K, M, N, d, persistent=True)
-    if not op.stats()["persistent"]:
-        pytest.skip("persistent passes unavailable on this device")
-    _steps(op, T, K, M)
-    for backward in (False, True):
-        tr = op.trace(backward)
-        passes = [e for e in tr if e["kind"] == "pass"]
-        assert len(passes) == 1 and passes[0]["tile"] == -1
-        assert sorted(_by(tr, "h2d")) == list(range(N))
     assert op.close() == tl.TL_OK
     for b in bufs:
         b.close()
