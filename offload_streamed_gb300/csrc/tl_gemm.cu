@@ -417,16 +417,33 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // the L2: the persistent CTAs drift apart in K, so a group's blocks must
 // share the cache with the streamed operand's slices in flight (32 MiB
 // measured best or equal for all three GEMMs at the GPT-scale tile, against
-// 16, 48, 64 and 128 MiB, under the power cap).
-void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int32_t* raster, int32_t* group) {
+// 16, 48, 64 and 128 MiB, under the power cap).  When a group is a single
+// block (long reductions: a 256-row block of the 64K-hidden layer's forward
+// is 32 MiB) and holds fewer tiles than the `concurrent` tiles in flight, one
+// wave of tiles spans several groups, which walk the streamed operand's K
+// slices together and read each slice from DRAM once: the streamed operand
+// is then read once per wave of groups, not once per group.  Measured at
+// the power cap, resident: that forward 1432-1438 -> 1561-1567 TFLOP/s.
+// With two blocks per group the same count misjudged the 64K dX (27 waves,
+// 1604 -> 1564 TFLOP/s), so groups of two or more keep the per-group count.
+void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int concurrent, int32_t* raster,
+                       int32_t* group) {
     constexpr double kL2Budget = 32.0 * 1024 * 1024;
     const double a_blk = double(tile_m) * double(k_dim) * 2;
     const double b_blk = double(kBlockN) * double(k_dim) * 2;
     const double a_tot = a_blk * num_m, b_tot = b_blk * num_n;
     const int gm = std::max(1, std::min(num_m, int(kL2Budget / a_blk)));
     const int gn = std::max(1, std::min(num_n, int(kL2Budget / b_blk)));
-    const double t0 = a_tot + b_tot * double((num_m + gm - 1) / gm);
-    const double t1 = b_tot + a_tot * double((num_n + gn - 1) / gn);
+    const double c = std::max(1, concurrent);
+    // passes of the streamed operand: one per group, or per wave of
+    // single-block groups
+    auto passes = [&](int groups, int group_blocks, int group_tiles) {
+        if (group_blocks > 1) return double(groups);
+        const double per_wave = std::max(1.0, std::floor(c / group_tiles));
+        return std::ceil(groups / per_wave);
+    };
+    const double t0 = a_tot + b_tot * passes((num_m + gm - 1) / gm, gm, gm * num_n);
+    const double t1 = b_tot + a_tot * passes((num_n + gn - 1) / gn, gn, gn * num_m);
     if (t1 < t0) {
         *raster = 1;
         *group = gn;
@@ -520,7 +537,8 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     kp.num_n = int32_t((g.n_dim + kBlockN - 1) / kBlockN);
     kp.num_k = int32_t((g.k_dim + kBlockK - 1) / kBlockK);
     kp.num_tiles = kp.num_m * kp.num_n;
-    choose_tile_order(g.k_dim, tile_m, kp.num_m, kp.num_n, &kp.raster, &kp.group);
+    const int slots = pair ? num_sms / 2 : num_sms;  // tiles in flight at once
+    choose_tile_order(g.k_dim, tile_m, kp.num_m, kp.num_n, slots, &kp.raster, &kp.group);
     kp.k_seg = g.nseg > 1 ? int32_t(g.k_seg) : INT32_MAX;
     kp.d = g.d;
     kp.ldd = g.ldd;
@@ -531,7 +549,6 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     kp.err = g.err;
     kp.tile_counter = g.tile_counter;
     kp.timeout_ns = g.timeout_ns;
-    const int slots = pair ? num_sms / 2 : num_sms;
     const int units = kp.num_tiles < slots ? kp.num_tiles : slots;
     const int grid = pair ? 2 * units : units;
 

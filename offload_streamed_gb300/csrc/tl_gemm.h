@@ -64,7 +64,8 @@ std::string gemm_check(const GemmDesc& g);
 cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std::string* why);
 
 // Shared host helpers (defined in tl_gemm.cu).
-void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int32_t* raster, int32_t* group);
+void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int concurrent, int32_t* raster,
+                       int32_t* group);
 bool cta_pair_enabled();
 
 // Tile shape of the kernel (exported for sizing and tests).
