@@ -49,6 +49,7 @@ struct KParams {
     int32_t m_dim, n_dim, k_dim;
     int32_t num_m, num_n, num_k, num_tiles;
     int32_t raster, group;  // tile order (see kc::tile_coords)
+    int32_t stream_shared;  // the streamed operand is read by several groups at once (see choose_tile_order)
     int32_t k_seg;          // reduction rows per B segment (INT32_MAX: one segment)
     void* d;
     int64_t ldd;
@@ -165,9 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_map(&map_b);
             for (int j = 1; j < GemmDesc::kMaxSeg && j * p.k_seg < p.k_dim; ++j) tma_prefetch_map(&segs.m[j - 1]);
             // the tile order keeps a group of A blocks (raster 0) or of B
-            // blocks (raster 1) in L2; the other operand streams through
-            const uint64_t pol_a = p.raster == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
-            const uint64_t pol_b = p.raster == 0 ? l2_policy_evict_first() : l2_policy_evict_last();
+            // blocks (raster 1) in L2; the other operand streams through,
+            // and leaves L2 first unless the groups in flight share it
+            const uint64_t pol_s = p.stream_shared ? l2_policy_evict_normal() : l2_policy_evict_first();
+            const uint64_t pol_a = p.raster == 0 ? l2_policy_evict_last() : pol_s;
+            const uint64_t pol_b = p.raster == 0 ? pol_s : l2_policy_evict_last();
             uint32_t fills = 0;
             bool ok = true;
             for (int it = 0; ok; ++it) {
@@ -417,17 +420,21 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // the L2: the persistent CTAs drift apart in K, so a group's blocks must
 // share the cache with the streamed operand's slices in flight (32 MiB
 // measured best or equal for all three GEMMs at the GPT-scale tile, against
-// 16, 48, 64 and 128 MiB, under the power cap).  When a group is a single
-// block (long reductions: a 256-row block of the 64K-hidden layer's forward
-// is 32 MiB) and holds fewer tiles than the `concurrent` tiles in flight, one
+// 16, 48, 64 and 128 MiB, under the power cap).
+// When a group holds fewer tiles than the `concurrent` tiles in flight (long
+// reductions, whose blocks are so large that a group holds one or two), one
 // wave of tiles spans several groups, which walk the streamed operand's K
 // slices together and read each slice from DRAM once: the streamed operand
-// is then read once per wave of groups, not once per group.  Measured at
-// the power cap, resident: that forward 1432-1438 -> 1561-1567 TFLOP/s.
-// With two blocks per group the same count misjudged the 64K dX (27 waves,
-// 1604 -> 1564 TFLOP/s), so groups of two or more keep the per-group count.
+// is then read once per wave of groups, not once per group, and its loads
+// keep the L2's normal eviction priority instead of evict-first
+// (`stream_shared`), or the groups after the first find it gone.  Measured
+// resident at the power cap against groups counted one by one with
+// evict-first: 64K-hidden forward 1520 -> 1726-1740 TFLOP/s (DRAM bytes per
+// launch 14.7 -> 4.5 GB), its dX 1604-1620 -> 1681 (18.1 -> 12.6 GB), the
+// 1T-width forward 1535-1551 -> 1582-1585; the GPT-scale GEMMs' groups exceed
+// a wave, and their order is unchanged.
 void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int concurrent, int32_t* raster,
-                       int32_t* group) {
+                       int32_t* group, int32_t* stream_shared) {
     constexpr double kL2Budget = 32.0 * 1024 * 1024;
     const double a_blk = double(tile_m) * double(k_dim) * 2;
     const double b_blk = double(kBlockN) * double(k_dim) * 2;
@@ -435,21 +442,21 @@ void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int conc
     const int gm = std::max(1, std::min(num_m, int(kL2Budget / a_blk)));
     const int gn = std::max(1, std::min(num_n, int(kL2Budget / b_blk)));
     const double c = std::max(1, concurrent);
-    // passes of the streamed operand: one per group, or per wave of
-    // single-block groups
-    auto passes = [&](int groups, int group_blocks, int group_tiles) {
-        if (group_blocks > 1) return double(groups);
+    // passes of the streamed operand: one per wave of groups
+    auto passes = [&](int groups, int group_tiles) {
         const double per_wave = std::max(1.0, std::floor(c / group_tiles));
         return std::ceil(groups / per_wave);
     };
-    const double t0 = a_tot + b_tot * passes((num_m + gm - 1) / gm, gm, gm * num_n);
-    const double t1 = b_tot + a_tot * passes((num_n + gn - 1) / gn, gn, gn * num_m);
+    const double t0 = a_tot + b_tot * passes((num_m + gm - 1) / gm, gm * num_n);
+    const double t1 = b_tot + a_tot * passes((num_n + gn - 1) / gn, gn * num_m);
     if (t1 < t0) {
         *raster = 1;
         *group = gn;
+        *stream_shared = gn * num_m < concurrent ? 1 : 0;
     } else {
         *raster = 0;
         *group = gm;
+        *stream_shared = gm * num_n < concurrent ? 1 : 0;
     }
 }
 
@@ -538,7 +545,7 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
     kp.num_k = int32_t((g.k_dim + kBlockK - 1) / kBlockK);
     kp.num_tiles = kp.num_m * kp.num_n;
     const int slots = pair ? num_sms / 2 : num_sms;  // tiles in flight at once
-    choose_tile_order(g.k_dim, tile_m, kp.num_m, kp.num_n, slots, &kp.raster, &kp.group);
+    choose_tile_order(g.k_dim, tile_m, kp.num_m, kp.num_n, slots, &kp.raster, &kp.group, &kp.stream_shared);
     kp.k_seg = g.nseg > 1 ? int32_t(g.k_seg) : INT32_MAX;
     kp.d = g.d;
     kp.ldd = g.ldd;

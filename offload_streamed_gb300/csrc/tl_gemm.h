@@ -65,7 +65,7 @@ cudaError_t gemm_launch(const GemmDesc& g, int num_sms, cudaStream_t stream, std
 
 // Shared host helpers (defined in tl_gemm.cu).
 void choose_tile_order(int64_t k_dim, int tile_m, int num_m, int num_n, int concurrent, int32_t* raster,
-                       int32_t* group);
+                       int32_t* group, int32_t* stream_shared);
 bool cta_pair_enabled();
 
 // Tile shape of the kernel (exported for sizing and tests).
