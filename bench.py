@@ -964,12 +964,18 @@ def step_bounds(T: int, K: int, M: int, R: float, link: dict) -> dict:
             "ait_h2d_flop_per_byte": RL.ait_h2d(T), "crossover_T": RL.crossover_tokens(R, bh)}
 
 
-def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: float, link: dict,
-                   t_copy_only: float | None, w_dev) -> dict:
+def mean_link(a: dict, b: dict) -> dict:
+    return {k: 0.5 * (a[k] + b[k]) if isinstance(a[k], float) else a[k] for k in a}
+
+
+def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: float, w_dev) -> dict:
     """One layer at depth d (-1: automatic) and T tokens: TFLOP/s over the
     mean step, the step roofline (tightest and per phase), exposed copy
     against the resident GEMMs and the copy schedule alone, the depth and
-    staging slots the handle used, and each GEMM kind's rate."""
+    staging slots the handle used, and each GEMM kind's rate.  The host link
+    is shared with the machine's other jobs and its speed drifts, so the
+    link and the copy schedule are measured right before and after the
+    point's streamed steps, and the point's roofline uses their mean."""
     import torch
 
     from offload_streamed_gb300 import roofline as RL
@@ -978,7 +984,9 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     y = torch.empty(T, M, dtype=torch.bfloat16, device="cuda")
     dx = torch.empty(T, K, dtype=torch.float32, device="cuda")
     op = tl.TiledLinear(K, M, N, d, wl.w, wl.dw, tile_major=True)
-    resident = w_dev is not None and t_copy_only
+    resident = w_dev is not None
+    link0 = measure_link(wl.w, wl.dw, 1 << 29, reps=2)
+    t_copy0 = time_copy_schedule(cfg, wl.w, wl.dw, reps=2)
     # the resident GEMMs are timed right before and right after the streamed
     # steps, and the two averaged: the power-capped clock drifts by a percent
     # or two over seconds, which at large T is as long as the whole copy
@@ -991,10 +999,16 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     ms, per_step, st = timed_steps(op, x, dy, y, dx, steps, warmup)
     assert op.close() == tl.TL_OK
     del y, dx
+    t_copy1 = time_copy_schedule(cfg, wl.w, wl.dw, reps=2)
+    link1 = measure_link(wl.w, wl.dw, 1 << 29, reps=2)
+    link = mean_link(link0, link1)
+    t_copy_only = 0.5 * (t_copy0 + t_copy1)
     flops = RL.step_flops(T, K, M)
     b = step_bounds(T, K, M, R, link)
     med = per_step[len(per_step) // 2]
     kr = kernel_rates(st, T, K, M, N)
+    fc, bc = max(st["fwd_timed_calls"], 1), max(st["bwd_timed_calls"], 1)
+    h2d_ms = st["sum_fwd_h2d_ms"] + st["sum_bwd_h2d_ms"]
     out = {"config": cfg["name"], "T": T, "K": K, "M": M, "N": N, "d": d, "depth": st["depth"],
            "staging_slots": st["staging_slots"], "steps": steps,
            "tflops": round(flops / (ms / 1e3) / 1e12, 1), "ms_per_step": round(ms, 3),
@@ -1002,19 +1016,28 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
            "step_roofline": {"tflops": round(b["roofline_tflops"], 1), "frac": round(b["t_roof_ms"] / ms, 4),
                              "bound_by": b["bound_by"]},
            "phase_roofline": {"tflops": round(b["phase_tflops"], 1), "frac": round(b["t_phase_ms"] / ms, 4)},
-           "kernels_tflops": {k: (round(v["tflops"], 1) if v["tflops"] else None) for k, v in kr.items()}}
+           "kernels_tflops": {k: (round(v["tflops"], 1) if v["tflops"] else None) for k, v in kr.items()},
+           "link_gbs_before_after": {"h2d": [round(link0["h2d_gbs"], 1), round(link1["h2d_gbs"], 1)],
+                                     "d2h": [round(link0["d2h_gbs"], 1), round(link1["d2h_gbs"], 1)],
+                                     "bidir_each": [round(link0["bidir_each_gbs"], 1),
+                                                    round(link1["bidir_each_gbs"], 1)]},
+           "link_gbs_during_steps": {
+               "h2d_per_copy": round((st["fwd_h2d_bytes"] + st["bwd_h2d_bytes"]) * fc / (h2d_ms / 1e3) / 1e9, 1)
+               if h2d_ms > 0 else None,
+               "d2h_per_copy": round(st["bwd_d2h_bytes"] * bc / (st["sum_bwd_d2h_ms"] / 1e3) / 1e9, 1)
+               if st["sum_bwd_d2h_ms"] > 0 else None}}
+    out["t_copy_only_ms"] = round(t_copy_only, 3)
     if resident:
         t_res1 = time_resident_compute(tl, cfg, x, dy, w_dev, res_steps, st["depth"])
         t_res = 0.5 * (t_res0 + t_res1)
         out["t_compute_resident_ms"] = round(t_res, 3)
         out["t_compute_resident_before_after_ms"] = [round(t_res0, 3), round(t_res1, 3)]
-        out["t_copy_only_ms"] = round(t_copy_only, 3)
         out["exposed_copy_pct"] = round(100.0 * max(0.0, ms - t_res) / t_copy_only, 2)
         out["exposed_copy_pct_median_step"] = round(100.0 * max(0.0, med - t_res) / t_copy_only, 2)
     return out
 
 
-def run_per_config(tl, args, R: float, link: dict, dist: Dist) -> dict:
+def run_per_config(tl, args, R: float, dist: Dist) -> dict:
     """The pages' other layers (PER_CONFIG), each workload built once and
     measured at its depths and token counts."""
     import torch
@@ -1026,11 +1049,9 @@ def run_per_config(tl, args, R: float, link: dict, dist: Dist) -> dict:
         T_alloc = max(T or cfg["T"] for _, T in pts)
         log(f"[bench] per-config {name}: T up to {T_alloc}, points {pts}")
         wl = Workload(cfg, args.seed, T_alloc)
-        t_copy = time_copy_schedule(cfg, wl.w, wl.dw)
         w_dev = w_device_rowmajor(wl.w, cfg["K"], cfg["M"], cfg["N"])
         for d, T in pts:
-            out.append(measure_config(tl, wl, cfg, d, T or cfg["T"], PER_CONFIG_STEPS, PER_CONFIG_WARMUP, R, link,
-                                      t_copy, w_dev))
+            out.append(measure_config(tl, wl, cfg, d, T or cfg["T"], PER_CONFIG_STEPS, PER_CONFIG_WARMUP, R, w_dev))
             log(f"[bench] {out[-1]}")
         del w_dev
         wl.close()
@@ -1038,9 +1059,11 @@ def run_per_config(tl, args, R: float, link: dict, dist: Dist) -> dict:
     return {"steps": PER_CONFIG_STEPS, "warmup": PER_CONFIG_WARMUP,
             "what": "each layer measured in this process like the headline (mean step over the timed steps); "
                     "d = -1 is the automatic depth, `depth` the one it chose and `staging_slots` the dW slots it "
-                    "carved; exposed_copy_pct against the same GEMMs on W resident in HBM and the copy schedule "
-                    "alone; step_roofline is max(6TKM/R, 4KM/B_h2d, 2KM/B_d2h), phase_roofline sums forward "
-                    "and backward bounds with the backward's links at their concurrent rates",
+                    "carved; exposed_copy_pct against the same GEMMs on W resident in HBM (timed before and after "
+                    "the streamed steps) and the copy schedule alone; step_roofline is max(6TKM/R, 4KM/B_h2d, "
+                    "2KM/B_d2h), phase_roofline sums forward and backward bounds with the backward's links at "
+                    "their concurrent rates, both with the link measured right before and after the point "
+                    "(the host link is shared with the machine's other jobs)",
             "points": out}
 
 
@@ -1088,6 +1111,7 @@ def run_ours(args, cfg, dist: Dist):
         dist.barrier()
         clocks["v"] = sampler.stop()
 
+    link_before = measure_link(wl.w, wl.dw, 1 << 30) if not args.skip_aux else None
     ms_local, per_step, st = timed_steps(op, x, dy, y, dx, args.steps, args.warmup, before, after)
     ms = dist.max(ms_local)
     launches = args.steps * (st["fwd_launches"] + st["bwd_launches"])
@@ -1150,9 +1174,9 @@ def run_ours(args, cfg, dist: Dist):
     out["clocks"] = clocks.get("v")
 
     # --- link, copy-only and resident-compute references; end to end -----------
-    link = None
     if not args.skip_aux:
-        link = measure_link(wl.w, wl.dw, 1 << 30)
+        link_after = measure_link(wl.w, wl.dw, 1 << 30)
+        link = mean_link(link_before, link_after)
         t_copy = time_copy_schedule(cfg, wl.w, wl.dw)
         w_dev = w_device_rowmajor(wl.w, K, M, N)
         t_res = time_resident_compute(tl, cfg, x, dy, w_dev, max(3, min(args.steps, 10)), st["depth"])
@@ -1183,6 +1207,9 @@ def run_ours(args, cfg, dist: Dist):
                           "t_bwd_ms": round(b["t_phase_bwd_ms"], 4), "roofline_tflops": round(b["phase_tflops"], 1),
                           "frac": round(b["t_phase_ms"] / ms_local, 4)}}
         out["link"] = {k: round(v, 1) if isinstance(v, float) else v for k, v in link.items()}
+        out["link"]["what"] = "pinned 1 GiB copies (h2d alone, d2h alone, each way while both run), the mean of " \
+                              "one measurement right before and one right after the timed steps"
+        out["link"]["before_after_h2d_gbs"] = [round(link_before["h2d_gbs"], 1), round(link_after["h2d_gbs"], 1)]
         e_ms, h2d, d2h = run_e2e(op, cfg, x, dy, max(3, min(args.steps, 20)), 2)
         e_ms = dist.max(e_ms)
         out["e2e"] = {"value": round(dist.world * flops_step / (e_ms / 1e3) / 1e12, 2), "unit": UNIT,
@@ -1208,7 +1235,7 @@ def run_ours(args, cfg, dist: Dist):
 
     # --- the pages' other layers ----------------------------------------------
     if not args.skip_aux and not args.no_per_config:
-        out["per_config"] = run_per_config(tl, args, R, link, dist)
+        out["per_config"] = run_per_config(tl, args, R, dist)
 
     # --- extensions on the GPT-scale layer, apart from the method's metric -------
     if not args.skip_aux:
@@ -1283,15 +1310,13 @@ def run_sweep(args, dist: Dist):
     T_max = max(SWEEP_T)
     log(f"[sweep] building workload (T up to {T_max}, K={cfg['K']}, M={cfg['M']}, N={cfg['N']})")
     wl = Workload(cfg, args.seed, T_max)
-    link = measure_link(wl.w, wl.dw, 1 << 30)
-    t_copy = time_copy_schedule(cfg, wl.w, wl.dw)
     w_dev = w_device_rowmajor(wl.w, cfg["K"], cfg["M"], cfg["N"])
     sampler = ClockSampler(None)
     sampler.start()
     points = []
     for d in SWEEP_D:
         for T in SWEEP_T:
-            points.append(measure_config(tl, wl, cfg, d, T, args.steps, args.warmup, R, link, t_copy, w_dev))
+            points.append(measure_config(tl, wl, cfg, d, T, args.steps, args.warmup, R, w_dev))
             log(f"[sweep] {points[-1]}")
     clocks = sampler.stop()
     del w_dev
@@ -1299,8 +1324,7 @@ def run_sweep(args, dist: Dist):
     return {"sweep": "ait", "metric": METRIC, "unit": UNIT, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": cfg["workload"], "K": cfg["K"], "M": cfg["M"], "N": cfg["N"], "T": SWEEP_T,
                        "d": SWEEP_D, "host_layout": "tile-major [N][K][M/N]"},
-            "link": {k: round(v, 1) if isinstance(v, float) else v for k, v in link.items()},
-            "R_tflops": peaks["bf16_tflops"], "t_copy_only_ms": round(t_copy, 3), "points": points,
+            "R_tflops": peaks["bf16_tflops"], "points": points,
             "clocks": clocks}
 
 
