@@ -1027,6 +1027,13 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
                "d2h_per_copy": round(st["bwd_d2h_bytes"] * bc / (st["sum_bwd_d2h_ms"] / 1e3) / 1e9, 1)
                if st["sum_bwd_d2h_ms"] > 0 else None}}
     out["t_copy_only_ms"] = round(t_copy_only, 3)
+    # how long the compute stream sat idle inside the timed calls (waiting
+    # for copies), as a share of the copy schedule: the part of the exposed
+    # copy that is waiting, not GEMMs slowed by the copies running beside them
+    gemm_ms = st["sum_fwd_gemm_ms"] + st["sum_bwd_dw_gemm_ms"] + st["sum_bwd_dx_gemm_ms"]
+    wait_ms = max(0.0, st["sum_fwd_total_ms"] + st["sum_bwd_total_ms"] - gemm_ms) / fc
+    out["compute_wait_ms_per_step"] = round(wait_ms, 3)
+    out["compute_wait_pct_of_copy"] = round(100.0 * wait_ms / t_copy_only, 2)
     if resident:
         t_res1 = time_resident_compute(tl, cfg, x, dy, w_dev, res_steps, st["depth"])
         t_res = 0.5 * (t_res0 + t_res1)
