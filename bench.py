@@ -351,11 +351,11 @@ def time_copy_schedule(cfg, w, dw, reps: int = 3):
 
 def dx_group(d: int, N: int, Mi: int) -> int:
     """Tiles per dX launch at depth d: the engine's rule (tiled_linear.h,
-    backward), max(2, ceil(8192 / Mi)) bounded by d + 1, N and 4."""
+    backward), max(2, ceil(8192 / Mi)) bounded by d, N and 4."""
     d = min(d, N - 1)
-    if d < 1 or N < 2 or Mi % 64:
+    if d < 2 or N < 2 or Mi % 64:
         return 1
-    return min(max(2, -(-8192 // Mi)), d + 1, N, 4)
+    return min(max(2, -(-8192 // Mi)), d, N, 4)
 
 
 def w_device_rowmajor(w, K: int, M: int, N: int):

@@ -196,8 +196,8 @@ tl_status tiled_linear_forward(tl_handle *h, int64_t T, const void *x_dev, void 
 /* Backward, tiles in descending order i = N-1 .. 0:
  *   dW_i = X^T . dY_i  (fp32 accumulation, bf16 RNE) -> dw_host tile i
  *   dx_dev[T, K] (fp32, ld K) = sum_i dY_i . W_i^T   (overwritten).  Fixed
- *   summation order: when d >= 1, N >= 2 and Mi % 64 == 0, tiles go in
- *   groups of g = min(max(2, ceil(8192 / Mi)), d+1, N, 4) consecutive tiles,
+ *   summation order: when min(d, N-1) >= 2 and Mi % 64 == 0, tiles go in
+ *   groups of g = min(max(2, ceil(8192 / Mi)), d, N-1, 4) consecutive tiles,
  *   (N-1 .. N-g), (N-g-1 .. N-2g), ..., the last group holding what is
  *   left; each group is reduced
  *   in one fp32 accumulator over its columns in ascending order, the first
@@ -400,7 +400,8 @@ size_t tiled_linear_chain_scratch_bytes(int64_t T, int32_t L, const int64_t *dim
  * (bf16 [T, dims[L]]) as its dY; operator l < L-1 takes the bf16 RNE of the
  * fp32 dX that operator l+1 produced.  Each operator's dW_l goes to its
  * dw_host as tiled_linear_backward writes it, and dx_dev (fp32 [T, dims[0]])
- * receives operator 0's dX.  y_dev[0..L-2] are the forward's outputs (the
+ * receives operator 0's dX.  Operator l sums its dX over the tile groups that
+ * tiled_linear_backward uses for n_tiles[l] tiles at depth d.  y_dev[0..L-2] are the forward's outputs (the
  * inputs X_1..X_{L-1}); for L = 1 y_dev may be NULL.  scratch_dev: 256-byte
  * aligned device memory of at least tiled_linear_chain_scratch_bytes(T, L,
  * dims) bytes (may be NULL for L = 1), used until `stream` completes.

@@ -244,19 +244,25 @@ tl_status finish_auto_depth(tl_handle* h) {
 namespace {
 
 // dX is accumulated over groups of consecutive tiles, one launch per group,
-// whenever the ring holds several tiles (d >= 1) and the tile width splits
-// into whole 64-deep K-blocks.  A group reduces at least 8192 deep where the
-// ring allows: g = max(2, ceil(8192 / Mi)), at most d + 1, N and 4 (the
-// GEMM's B segments); the last group of an operator may be smaller.  Pairs
-// for wide tiles: a larger group holds more of the ring and delays the next
-// fetches (groups of three measured 1 % slower on the GPT-scale layer), while
-// narrow tiles need the depth (groups of three: +7 % on the FFN chain, whose
-// down-projection has 1024-wide tiles).  Both launch modes use the same
-// groups, so their dX agree bit for bit.
+// whenever the operator's depth min(d, N - 1) is at least 2 and the tile
+// width splits into whole 64-deep K-blocks.  A group reduces at least 8192
+// deep where the ring allows: g = max(2, ceil(8192 / Mi)), at most
+// min(d, N - 1) and 4 (the GEMM's B segments); the last group of an
+// operator may be smaller.  The bound uses the operator's own N, so that an
+// operator groups its tiles the same way alone and inside a chain.
+// A group holds its tiles' ring slots until its launch, so g <= d leaves at
+// least one of the d + 1 slots fetching ahead while the group computes: at
+// d = 1 a pair would hold the whole ring and stop the refetch during each dX
+// launch (1T-width layer at d = 1: 994 TFLOP/s with pairs, 1155 with single
+// tiles; the link-bound sweep point T = 2048 at d = 1: +6 to 8 %).  Larger
+// groups mean fewer fp32 passes over dX; pairs stay for wide tiles (groups of
+// three measured 1 % slower on the GPT-scale layer).  Both launch modes use
+// the same groups, so their dX agree bit for bit.
 int dx_group(const tl_handle* h, const Shape& s) {
-    if (h->d < 1 || s.N < 2 || s.Mi % tl::kBlockK) return 1;
+    const int d = std::min(h->d, s.N - 1);
+    if (d < 2 || s.Mi % tl::kBlockK) return 1;
     const int want = std::max<int>(2, int((8192 + s.Mi - 1) / s.Mi));
-    return std::min({want, h->d + 1, s.N, int(tl::GemmDesc::kMaxSeg)});
+    return std::min({want, d, int(tl::GemmDesc::kMaxSeg)});
 }
 
 tl_status launch(tl_handle* h, const tl::GemmDesc& g0, cudaStream_t st) {

@@ -45,11 +45,13 @@ def test_union_and_overlap():
     assert bench._overlap([], [[0, 1]]) == 0.0
 
 
-@pytest.mark.parametrize("d,N,Mi,g", [(2, 8, 4096, 2), (2, 8, 1024, 3), (3, 16, 1024, 4), (0, 8, 4096, 1),
-                                      (5, 1, 4096, 1), (2, 8, 100, 1), (4, 8, 8192, 2), (1, 4, 256, 2)])
+@pytest.mark.parametrize("d,N,Mi,g", [(2, 8, 4096, 2), (2, 8, 1024, 2), (3, 16, 1024, 3), (4, 16, 1024, 4),
+                                      (9, 16, 256, 4), (0, 8, 4096, 1), (1, 4, 256, 1), (1, 16, 6400, 1),
+                                      (5, 1, 4096, 1), (2, 8, 100, 1), (4, 8, 8192, 2), (3, 3, 1024, 2)])
 def test_dx_group_rule(d, N, Mi, g):
-    """max(2, ceil(8192 / Mi)) bounded by d + 1, N and 4; one tile when the
-    ring holds one tile or Mi is not a multiple of 64."""
+    """max(2, ceil(8192 / Mi)) bounded by d, N and 4 (d clamped to N - 1);
+    one tile when the ring holds at most two tiles or Mi is not a multiple
+    of 64."""
     assert bench.dx_group(d, N, Mi) == g
 
 

@@ -47,9 +47,9 @@ def _sampled_parity(T, K, M, N, x_bits, dy_bits, w_tm, y, dx, dw_tm, seed):
 def _dx_group(d, N, Mi):
     """Tiles per dX group for depth d (the engine's rule)."""
     d = min(d, N - 1)
-    if not (d >= 1 and N >= 2 and Mi % 64 == 0):
+    if not (d >= 2 and N >= 2 and Mi % 64 == 0):
         return 1
-    return min(max(2, -(-8192 // Mi)), d + 1, N, 4)
+    return min(max(2, -(-8192 // Mi)), d, N, 4)
 
 
 def _run_config(tl, T, K, M, N, depths, seed=0, untiled=True):
