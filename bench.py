@@ -27,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -66,7 +67,11 @@ HEADLINE = "64k"  # the largest configuration that fits one GPU
 PER_CONFIG = [("gpt", 2, None), ("1t", 1, None), ("1t", 2, None), ("1t", 3, None),
               ("sweep", -1, 2048), ("sweep", -1, 4096), ("sweep", -1, 8192), ("sweep", -1, 65536),
               ("sweep", 4, 65536), ("sweep", 8, 65536), ("sweep", 15, 65536)]
-PER_CONFIG_STEPS, PER_CONFIG_WARMUP = 10, 3
+PER_CONFIG_STEPS, PER_CONFIG_WARMUP = 4, 2
+# each per-config block (streamed steps, resident GEMMs) times at least this
+# long, after a warm-up of at least this long, so that both blocks settle at
+# the clock the power budget gives that work
+PER_CONFIG_SECONDS, PER_CONFIG_WARM_SECONDS = 0.3, 0.15
 
 TIMING_EVERY = 4
 
@@ -371,11 +376,11 @@ def w_device_rowmajor(w, K: int, M: int, N: int):
     return w_dev
 
 
-def time_resident_compute(tl, cfg, x, dy, w_dev, steps: int, depth: int):
+def time_resident_compute(tl, cfg, x, dy, w_dev, steps: int, depth: int, warmup: int = 2):
     """t_compute_resident: the step's GEMM sequence (the same kernels, same
     order, dX over the same tile groups as at `depth`) on W already in HBM
     (row-major [K, M], so a group of tiles is one column block), through the
-    resident-GEMM ABI."""
+    resident-GEMM ABI; `warmup` untimed steps first."""
     import torch
     T, K, M, N = x.shape[0], cfg["K"], cfg["M"], cfg["N"]
     Mi = M // N
@@ -404,7 +409,7 @@ def time_resident_compute(tl, cfg, x, dy, w_dev, steps: int, depth: int):
                                     dx.data_ptr(), K, nx > 0, err.data_ptr(), st)
             nx, pend = nx + 1, 0
 
-    for _ in range(2):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -975,7 +980,9 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     staging slots the handle used, and each GEMM kind's rate.  The host link
     is shared with the machine's other jobs and its speed drifts, so the
     link and the copy schedule are measured right before and after the
-    point's streamed steps, and the point's roofline uses their mean."""
+    point's streamed steps, and the point's roofline uses their mean.
+    `steps` and `warmup` are minimums: each block runs at least
+    PER_CONFIG_SECONDS after at least PER_CONFIG_WARM_SECONDS of warm-up."""
     import torch
 
     from offload_streamed_gb300 import roofline as RL
@@ -987,16 +994,29 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     resident = w_dev is not None
     link0 = measure_link(wl.w, wl.dw, 1 << 29, reps=2)
     t_copy0 = time_copy_schedule(cfg, wl.w, wl.dw, reps=2)
-    # the resident GEMMs are timed right before and right after the streamed
-    # steps, and the two averaged: the power-capped clock drifts by a percent
-    # or two over seconds, which at large T is as long as the whole copy
-    # schedule
-    res_steps = max(3, steps // 2)
+    # the automatic depth is chosen after the first forward and used from the
+    # second; one streamed step then sizes the blocks
+    op.forward(x, y)
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    op.forward(x, y, stream=s)
+    op.backward(x, dy, dx, stream=s)
+    e1.record(s)
+    torch.cuda.synchronize()
+    est = max(e0.elapsed_time(e1), 1e-3)
+    steps = max(steps, math.ceil(PER_CONFIG_SECONDS * 1e3 / est))
+    warmup = max(warmup, math.ceil(PER_CONFIG_WARM_SECONDS * 1e3 / est))
+    depth = op.stats()["depth"]
+    # The resident GEMMs run right before and right after the streamed
+    # steps, with the same warm-up and at least as many timed steps, and
+    # the two are averaged: each block settles at the clock the power budget
+    # gives its own work, and the clock's drift over seconds cancels
     if resident:
-        op.forward(x, y)  # the automatic depth is chosen after the first forward, used from the second
-        op.forward(x, y)
-        t_res0 = time_resident_compute(tl, cfg, x, dy, w_dev, res_steps, op.stats()["depth"])
+        t_res0 = time_resident_compute(tl, cfg, x, dy, w_dev, steps, depth, warmup)
     ms, per_step, st = timed_steps(op, x, dy, y, dx, steps, warmup)
+    if resident:
+        t_res1 = time_resident_compute(tl, cfg, x, dy, w_dev, steps, st["depth"], warmup)
     assert op.close() == tl.TL_OK
     del y, dx
     t_copy1 = time_copy_schedule(cfg, wl.w, wl.dw, reps=2)
@@ -1010,7 +1030,7 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     fc, bc = max(st["fwd_timed_calls"], 1), max(st["bwd_timed_calls"], 1)
     h2d_ms = st["sum_fwd_h2d_ms"] + st["sum_bwd_h2d_ms"]
     out = {"config": cfg["name"], "T": T, "K": K, "M": M, "N": N, "d": d, "depth": st["depth"],
-           "staging_slots": st["staging_slots"], "steps": steps,
+           "staging_slots": st["staging_slots"], "steps": steps, "warmup": warmup,
            "tflops": round(flops / (ms / 1e3) / 1e12, 1), "ms_per_step": round(ms, 3),
            "step_ms_median": round(med, 3), "step_ms_max": round(per_step[-1], 3),
            "step_roofline": {"tflops": round(b["roofline_tflops"], 1), "frac": round(b["t_roof_ms"] / ms, 4),
@@ -1035,7 +1055,6 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     out["compute_wait_ms_per_step"] = round(wait_ms, 3)
     out["compute_wait_pct_of_copy"] = round(100.0 * wait_ms / t_copy_only, 2)
     if resident:
-        t_res1 = time_resident_compute(tl, cfg, x, dy, w_dev, res_steps, st["depth"])
         t_res = 0.5 * (t_res0 + t_res1)
         out["t_compute_resident_ms"] = round(t_res, 3)
         out["t_compute_resident_before_after_ms"] = [round(t_res0, 3), round(t_res1, 3)]
@@ -1063,11 +1082,14 @@ def run_per_config(tl, args, R: float, dist: Dist) -> dict:
         del w_dev
         wl.close()
     torch.cuda.synchronize()
-    return {"steps": PER_CONFIG_STEPS, "warmup": PER_CONFIG_WARMUP,
-            "what": "each layer measured in this process like the headline (mean step over the timed steps); "
+    return {"min_steps": PER_CONFIG_STEPS, "min_warmup": PER_CONFIG_WARMUP,
+            "min_block_s": PER_CONFIG_SECONDS, "min_warmup_s": PER_CONFIG_WARM_SECONDS,
+            "what": "each layer measured in this process like the headline (mean step over the timed steps, "
+                    "each point's `steps` and `warmup` sized to at least min_block_s and min_warmup_s); "
                     "d = -1 is the automatic depth, `depth` the one it chose and `staging_slots` the dW slots it "
-                    "carved; exposed_copy_pct against the same GEMMs on W resident in HBM (timed before and after "
-                    "the streamed steps) and the copy schedule alone; step_roofline is max(6TKM/R, 4KM/B_h2d, "
+                    "carved; exposed_copy_pct against the same GEMMs on W resident in HBM (timed right before and "
+                    "right after the streamed steps, each block as long and as warmed up as the streamed one) "
+                    "and the copy schedule alone; step_roofline is max(6TKM/R, 4KM/B_h2d, "
                     "2KM/B_d2h), phase_roofline sums forward and backward bounds with the backward's links at "
                     "their concurrent rates, both with the link measured right before and after the point "
                     "(the host link is shared with the machine's other jobs)",
