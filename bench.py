@@ -1326,6 +1326,13 @@ def run_sweep(args, dist: Dist):
     exposed copy against the same GEMMs on resident W and the same copies
     alone.  The link hides behind compute once ait = 1.5 T FLOP/B passes
     R / B_h2d (tm_zero_infinity, "The honest cost")."""
+    try:
+        depths = [int(v) for v in args.sweep_d.split(",")] if args.sweep_d else SWEEP_D
+        tokens = [int(v) for v in args.sweep_t.split(",")] if args.sweep_t else SWEEP_T
+    except ValueError:
+        depths = tokens = []
+    if not depths or not tokens or any(d < -1 for d in depths) or any(not 1 <= T <= max(SWEEP_T) for T in tokens):
+        raise SystemExit(f"--sweep-d / --sweep-t: integer depths >= -1 and token counts in 1..{max(SWEEP_T)}")
     import torch
 
     import __graft_entry__ as g
@@ -1336,23 +1343,23 @@ def run_sweep(args, dist: Dist):
     peaks = load_peaks()
     R = peaks["bf16_tflops"] * 1e12
     cfg = dict(CONFIGS["sweep"], name="sweep")
-    T_max = max(SWEEP_T)
+    T_max = max(tokens)
     log(f"[sweep] building workload (T up to {T_max}, K={cfg['K']}, M={cfg['M']}, N={cfg['N']})")
     wl = Workload(cfg, args.seed, T_max)
     w_dev = w_device_rowmajor(wl.w, cfg["K"], cfg["M"], cfg["N"])
     sampler = ClockSampler(None)
     sampler.start()
     points = []
-    for d in SWEEP_D:
-        for T in SWEEP_T:
+    for d in depths:
+        for T in tokens:
             points.append(measure_config(tl, wl, cfg, d, T, args.steps, args.warmup, R, w_dev))
             log(f"[sweep] {points[-1]}")
     clocks = sampler.stop()
     del w_dev
     wl.close()
     return {"sweep": "ait", "metric": METRIC, "unit": UNIT, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": cfg["workload"], "K": cfg["K"], "M": cfg["M"], "N": cfg["N"], "T": SWEEP_T,
-                       "d": SWEEP_D, "host_layout": "tile-major [N][K][M/N]"},
+            "config": {"workload": cfg["workload"], "K": cfg["K"], "M": cfg["M"], "N": cfg["N"], "T": tokens,
+                       "d": depths, "host_layout": "tile-major [N][K][M/N]"},
             "R_tflops": peaks["bf16_tflops"], "points": points,
             "clocks": clocks}
 
@@ -1420,6 +1427,10 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time the arithmetic-intensity sweep (K=16384, M=65536, N=16; T = 512..65536, "
                          "d = 1..4 and automatic) and print one JSON line with every point")
+    ap.add_argument("--sweep-d", type=str, default=None, metavar="D,...",
+                    help="with --sweep: only these depths (-1 = automatic), e.g. 3,4,-1")
+    ap.add_argument("--sweep-t", type=str, default=None, metavar="T,...",
+                    help="with --sweep: only these token counts (each in 1..65536)")
     ap.add_argument("--profile-gemms", type=int, default=0, metavar="R",
                     help="only run the resident GEMMs of one tile R times (for ncu), print nothing")
     ap.add_argument("--profile-kinds", default="fwd,dw,dx", help="kernels --profile-gemms runs")
