@@ -1241,8 +1241,15 @@ def run_ours(args, cfg, dist: Dist):
         out["link"]["before_after_h2d_gbs"] = [round(link_before["h2d_gbs"], 1), round(link_after["h2d_gbs"], 1)]
         e_ms, h2d, d2h = run_e2e(op, cfg, x, dy, max(3, min(args.steps, 20)), 2)
         e_ms = dist.max(e_ms)
+        t_e2e = RL.e2e_bound(T, K, M, R, h2d, d2h, link["h2d_gbs"] * 1e9, link["d2h_gbs"] * 1e9,
+                             link["bidir_each_gbs"] * 1e9)
         out["e2e"] = {"value": round(dist.world * flops_step / (e_ms / 1e3) / 1e12, 2), "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4),
+                      "roofline": {"form": "t = max(6TKM/R, link time of (4KM + in) bytes in and (2KM + out) "
+                                           "bytes out, both directions together at B_bidir for the smaller "
+                                           "amount, the rest alone)",
+                                   "t_ms": round(t_e2e * 1e3, 4), "tflops": round(flops_step / t_e2e / 1e12, 1),
+                                   "frac": round(t_e2e * 1e3 / e_ms, 4)},
                       # the weight tiles the step streams besides (W in twice, dW out once)
                       "weight_h2d_bytes_per_step": int(RL.step_h2d_bytes(K, M)),
                       "weight_d2h_bytes_per_step": int(RL.step_d2h_bytes(K, M)),

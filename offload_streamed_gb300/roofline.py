@@ -72,6 +72,29 @@ def phase_bound(T: int, K: int, M: int, R: float, B_h2d: float, B_h2d_bidir: flo
     return t_f, t_b
 
 
+def link_seconds(h2d_bytes: float, d2h_bytes: float, B_h2d: float, B_d2h: float, B_bidir: float) -> float:
+    """Shortest time the host link needs to move h2d_bytes in and d2h_bytes
+    out, with each direction at its solo rate (B_h2d, B_d2h) while it runs
+    alone and both at B_bidir each while both run: the two directions run
+    together for the smaller amount and the larger one's remainder runs
+    alone (when 2 B_bidir is at least either solo rate, as it is on this
+    link, overlapping them is never slower)."""
+    both = min(h2d_bytes, d2h_bytes)
+    return both / B_bidir + (h2d_bytes - both) / B_h2d + (d2h_bytes - both) / B_d2h
+
+
+def e2e_bound(T: int, K: int, M: int, R: float, act_in: float, act_out: float, B_h2d: float, B_d2h: float,
+              B_bidir: float) -> float:
+    """A step whose activations also cross the host link (act_in bytes in,
+    act_out bytes out, besides the weights' 4 K M in and 2 K M out): no
+    faster than its FLOPs at R or its link traffic (link_seconds), whichever
+    takes longer.  With no activations and a link-bound step this is the
+    per-phase bound's link time, since the weights' bytes already fill the
+    backward's two directions equally."""
+    return max(step_flops(T, K, M) / R,
+               link_seconds(step_h2d_bytes(K, M) + act_in, step_d2h_bytes(K, M) + act_out, B_h2d, B_d2h, B_bidir))
+
+
 def gemm_flops(T: int, K: int, n: int) -> float:
     """One tile GEMM: forward, dW and dX each do 2 T K n FLOPs over a tile (or
     tile group) of n weight columns."""

@@ -100,6 +100,37 @@ def test_phase_bound_matches_phase_serial_schedule(T, R, bh, bd):
     assert t_f + t_b >= RL.step_bound(T, K, M, R, bh, bd)[0] * (1 - 1e-12)
 
 
+@pytest.mark.parametrize("h,d,bh,bd,bb", [(5e9, 2e9, 2.1e11, 1.9e11, 1.7e11), (1e9, 3e9, 2.1e11, 1.9e11, 1.7e11),
+                                         (4e9, 4e9, 2e11, 2e11, 1.2e11), (3e9, 0.0, 2e11, 1e11, 1e11)])
+def test_link_seconds_is_the_best_time_sharing_schedule(h, d, bh, bd, bb):
+    """Brute force over schedules that spend t_c with both directions running
+    (B_bidir each), t_h with host->device alone and t_d with device->host
+    alone: the least t_c + t_h + t_d that moves both amounts."""
+    best = float("inf")
+    top = min(h, d) / bb
+    for j in range(2001):
+        t_c = top * j / 2000
+        t = t_c + max(0.0, h - bb * t_c) / bh + max(0.0, d - bb * t_c) / bd
+        best = min(best, t)
+    assert RL.link_seconds(h, d, bh, bd, bb) == pytest.approx(best, rel=1e-9)
+
+
+def test_e2e_bound():
+    T, K, M, R = 2048, 65536, 262144, 1.936e15
+    bh, bd, bb = 2.1e11, 1.92e11, 1.7e11
+    w = 2.0 * K * M
+    # no activations: the per-phase bound's link time (W in alone, then W in and dW out together)
+    t_f, t_b = RL.phase_bound(T, K, M, R, bh, bb, bb)
+    assert RL.e2e_bound(T, K, M, R, 0.0, 0.0, bh, bd, bb) == pytest.approx(t_f + t_b, rel=1e-12)
+    # activations: X, dY in and Y, dX (fp32) out, each byte at the rate of the direction it shares
+    a_in, a_out = 2.0 * T * (K + M), 2.0 * T * M + 4.0 * T * K
+    t = RL.e2e_bound(T, K, M, R, a_in, a_out, bh, bd, bb)
+    assert t == pytest.approx((w + a_out) / bb + (2 * w + a_in - w - a_out) / bh, rel=1e-12)
+    # compute-bound: the FLOPs at R
+    assert RL.e2e_bound(65536, 1024, 1024, 1e12, 1.0, 1.0, bh, bd, bb) == pytest.approx(
+        RL.step_flops(65536, 1024, 1024) / 1e12)
+
+
 def test_gemm_accounting():
     # one tile GEMM of each kind does a third of the tile's step FLOPs
     T, K, M, N = 8192, 8192, 32768, 8
