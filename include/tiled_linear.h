@@ -202,7 +202,8 @@ tl_status tiled_linear_forward(tl_handle *h, int64_t T, const void *x_dev, void 
  *   left; each group is reduced
  *   in one fp32 accumulator over its columns in ascending order, the first
  *   group stores, later groups add.  Otherwise the first tile stores and
- *   later tiles add one at a time.  Both launch modes use this order.
+ *   later tiles add one at a time.  The order depends on (N, Mi, d) alone,
+ *   not on the schedule (host layout, tile reuse, copy timing).
  * dy_dev is [T, M] bf16 (ld M).  T = 0 writes dW = 0.  dW on the host is
  * complete once `stream` has completed.  Errors as tiled_linear_forward. */
 tl_status tiled_linear_backward(tl_handle *h, int64_t T, const void *x_dev,

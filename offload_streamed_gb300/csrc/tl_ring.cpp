@@ -256,8 +256,9 @@ namespace {
 // launch (1T-width layer at d = 1: 994 TFLOP/s with pairs, 1155 with single
 // tiles; the link-bound sweep point T = 2048 at d = 1: +6 to 8 %).  Larger
 // groups mean fewer fp32 passes over dX; pairs stay for wide tiles (groups of
-// three measured 1 % slower on the GPT-scale layer).  Both launch modes use
-// the same groups, so their dX agree bit for bit.
+// three measured 1 % slower on the GPT-scale layer).  The groups depend on
+// (N, Mi, d) alone, so a backward that reuses resident tiles and one that
+// fetches them again agree bit for bit.
 int dx_group(const tl_handle* h, const Shape& s) {
     const int d = std::min(h->d, s.N - 1);
     if (d < 2 || s.Mi % tl::kBlockK) return 1;

@@ -110,7 +110,7 @@ def _same(a, b):
 
 def dx_group(depth, N, Mi):
     """Tiles per dX accumulation group for the depth a call ran with (from its
-    stats): both launch modes reduce dX over groups of
+    stats): the engine reduces dX over groups of
     min(max(2, ceil(8192 / Mi)), depth, N, 4) tiles whenever the ring holds
     more than two (depth >= 2) and the tile width is a multiple of 64;
     otherwise one tile at a time."""
