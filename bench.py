@@ -973,7 +973,8 @@ def mean_link(a: dict, b: dict) -> dict:
     return {k: 0.5 * (a[k] + b[k]) if isinstance(a[k], float) else a[k] for k in a}
 
 
-def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: float, w_dev) -> dict:
+def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: float, w_dev,
+                   R_sustained: float | None = None) -> dict:
     """One layer at depth d (-1: automatic) and T tokens: TFLOP/s over the
     mean step, the step roofline (tightest and per phase), exposed copy
     against the resident GEMMs and the copy schedule alone, the depth and
@@ -982,7 +983,9 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     link and the copy schedule are measured right before and after the
     point's streamed steps, and the point's roofline uses their mean.
     `steps` and `warmup` are minimums: each block runs at least
-    PER_CONFIG_SECONDS after at least PER_CONFIG_WARM_SECONDS of warm-up."""
+    PER_CONFIG_SECONDS after at least PER_CONFIG_WARM_SECONDS of warm-up.
+    With R_sustained, the step roofline is also given against the sustained
+    bf16 peak (the blocks run long enough to reach the power cap)."""
     import torch
 
     from offload_streamed_gb300 import roofline as RL
@@ -1033,6 +1036,9 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
            "staging_slots": st["staging_slots"], "steps": steps, "warmup": warmup,
            "tflops": round(flops / (ms / 1e3) / 1e12, 1), "ms_per_step": round(ms, 3),
            "step_ms_median": round(med, 3), "step_ms_max": round(per_step[-1], 3),
+           # the same at the median step: a stall of the shared host link
+           # (tens of ms, now and then) moves the mean of a short block
+           "tflops_median_step": round(flops / (med / 1e3) / 1e12, 1),
            "step_roofline": {"tflops": round(b["roofline_tflops"], 1), "frac": round(b["t_roof_ms"] / ms, 4),
                              "bound_by": b["bound_by"]},
            "phase_roofline": {"tflops": round(b["phase_tflops"], 1), "frac": round(b["t_phase_ms"] / ms, 4)},
@@ -1046,6 +1052,11 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
                if h2d_ms > 0 else None,
                "d2h_per_copy": round(st["bwd_d2h_bytes"] * bc / (st["sum_bwd_d2h_ms"] / 1e3) / 1e9, 1)
                if st["sum_bwd_d2h_ms"] > 0 else None}}
+    if R_sustained:
+        bs = step_bounds(T, K, M, R_sustained, link)
+        out["step_roofline"]["sustained"] = {"R_tflops": round(R_sustained / 1e12, 1),
+                                             "tflops": round(bs["roofline_tflops"], 1),
+                                             "frac": round(bs["t_roof_ms"] / ms, 4), "bound_by": bs["bound_by"]}
     out["t_copy_only_ms"] = round(t_copy_only, 3)
     # how long the compute stream sat idle inside the timed calls (waiting
     # for copies), as a share of the copy schedule: the part of the exposed
@@ -1063,7 +1074,7 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     return out
 
 
-def run_per_config(tl, args, R: float, dist: Dist) -> dict:
+def run_per_config(tl, args, R: float, dist: Dist, R_sustained: float | None = None) -> dict:
     """The pages' other layers (PER_CONFIG), each workload built once and
     measured at its depths and token counts."""
     import torch
@@ -1077,7 +1088,8 @@ def run_per_config(tl, args, R: float, dist: Dist) -> dict:
         wl = Workload(cfg, args.seed, T_alloc)
         w_dev = w_device_rowmajor(wl.w, cfg["K"], cfg["M"], cfg["N"])
         for d, T in pts:
-            out.append(measure_config(tl, wl, cfg, d, T or cfg["T"], PER_CONFIG_STEPS, PER_CONFIG_WARMUP, R, w_dev))
+            out.append(measure_config(tl, wl, cfg, d, T or cfg["T"], PER_CONFIG_STEPS, PER_CONFIG_WARMUP, R, w_dev,
+                                      R_sustained))
             log(f"[bench] {out[-1]}")
         del w_dev
         wl.close()
@@ -1090,7 +1102,9 @@ def run_per_config(tl, args, R: float, dist: Dist) -> dict:
                     "carved; exposed_copy_pct against the same GEMMs on W resident in HBM (timed right before and "
                     "right after the streamed steps, each block as long and as warmed up as the streamed one) "
                     "and the copy schedule alone; step_roofline is max(6TKM/R, 4KM/B_h2d, "
-                    "2KM/B_d2h), phase_roofline sums forward and backward bounds with the backward's links at "
+                    "2KM/B_d2h) with R the burst bf16 peak (`sustained`: the same with the sustained one, which "
+                    "these blocks run long enough to meet), phase_roofline sums forward and backward bounds "
+                    "with the backward's links at "
                     "their concurrent rates, both with the link measured right before and after the point "
                     "(the host link is shared with the machine's other jobs)",
             "points": out}
@@ -1271,7 +1285,7 @@ def run_ours(args, cfg, dist: Dist):
 
     # --- the pages' other layers ----------------------------------------------
     if not args.skip_aux and not args.no_per_config:
-        out["per_config"] = run_per_config(tl, args, R, dist)
+        out["per_config"] = run_per_config(tl, args, R, dist, peaks["bf16_tflops_sustained"] * 1e12)
 
     # --- extensions on the GPT-scale layer, apart from the method's metric -------
     if not args.skip_aux:
@@ -1359,7 +1373,8 @@ def run_sweep(args, dist: Dist):
     points = []
     for d in depths:
         for T in tokens:
-            points.append(measure_config(tl, wl, cfg, d, T, args.steps, args.warmup, R, w_dev))
+            points.append(measure_config(tl, wl, cfg, d, T, args.steps, args.warmup, R, w_dev,
+                                         peaks["bf16_tflops_sustained"] * 1e12))
             log(f"[sweep] {points[-1]}")
     clocks = sampler.stop()
     del w_dev
