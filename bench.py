@@ -67,7 +67,7 @@ HEADLINE = "64k"  # the largest configuration that fits one GPU
 PER_CONFIG = [("gpt", 2, None), ("1t", 1, None), ("1t", 2, None), ("1t", 3, None),
               ("sweep", -1, 2048), ("sweep", -1, 4096), ("sweep", -1, 8192), ("sweep", -1, 65536),
               ("sweep", 4, 65536), ("sweep", 8, 65536), ("sweep", 15, 65536)]
-PER_CONFIG_STEPS, PER_CONFIG_WARMUP = 4, 2
+PER_CONFIG_STEPS, PER_CONFIG_WARMUP = 6, 2
 # each per-config block (streamed steps, resident GEMMs) times at least this
 # long, after a warm-up of at least this long, so that both blocks settle at
 # the clock the power budget gives that work
