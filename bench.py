@@ -973,6 +973,16 @@ def mean_link(a: dict, b: dict) -> dict:
     return {k: 0.5 * (a[k] + b[k]) if isinstance(a[k], float) else a[k] for k in a}
 
 
+def block_sizes(step_ms: float, steps: int, warmup: int) -> tuple[int, int]:
+    """Timed steps and warm-up steps of one per-config block, from one
+    step's time: at least `steps` and `warmup`, and at least
+    PER_CONFIG_SECONDS of timed steps after PER_CONFIG_WARM_SECONDS of
+    warm-up."""
+    est = max(step_ms, 1e-3)
+    return (max(steps, math.ceil(PER_CONFIG_SECONDS * 1e3 / est)),
+            max(warmup, math.ceil(PER_CONFIG_WARM_SECONDS * 1e3 / est)))
+
+
 def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: float, w_dev,
                    R_sustained: float | None = None) -> dict:
     """One layer at depth d (-1: automatic) and T tokens: TFLOP/s over the
@@ -1007,9 +1017,7 @@ def measure_config(tl, wl, cfg, d: int, T: int, steps: int, warmup: int, R: floa
     op.backward(x, dy, dx, stream=s)
     e1.record(s)
     torch.cuda.synchronize()
-    est = max(e0.elapsed_time(e1), 1e-3)
-    steps = max(steps, math.ceil(PER_CONFIG_SECONDS * 1e3 / est))
-    warmup = max(warmup, math.ceil(PER_CONFIG_WARM_SECONDS * 1e3 / est))
+    steps, warmup = block_sizes(e0.elapsed_time(e1), steps, warmup)
     depth = op.stats()["depth"]
     # The resident GEMMs run right before and right after the streamed
     # steps, with the same warm-up and at least as many timed steps, and

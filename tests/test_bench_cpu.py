@@ -83,3 +83,13 @@ def test_extension_guard_reraises_with_several_ranks_and_on_cuda_errors():
         raise tl.TiledLinearError(tl.TL_ERR_CUDA, "x")
     with pytest.raises(tl.TiledLinearError):
         bench._extension(cuda, _OneRank())
+
+
+def test_block_sizes():
+    """Per-config blocks: at least the given counts, and at least 0.3 s of
+    timed steps after 0.15 s of warm-up."""
+    assert bench.block_sizes(8.0, 6, 2) == (38, 19)        # an 8 ms step: 0.3 s and 0.15 s decide
+    assert bench.block_sizes(250.0, 6, 2) == (6, 2)        # a 250 ms step: the minimum counts decide
+    assert bench.block_sizes(0.0, 6, 2)[0] >= 6            # a zero reading does not divide by zero
+    s, w = bench.block_sizes(23.0, 6, 2)
+    assert s * 23.0 >= 300.0 and w * 23.0 >= 150.0 and (s - 1) * 23.0 < 300.0
