@@ -977,8 +977,8 @@ def block_sizes(step_ms: float, steps: int, warmup: int) -> tuple[int, int]:
     """Timed steps and warm-up steps of one per-config block, from one
     step's time: at least `steps` and `warmup`, and at least
     PER_CONFIG_SECONDS of timed steps after PER_CONFIG_WARM_SECONDS of
-    warm-up."""
-    est = max(step_ms, 1e-3)
+    warm-up (a step read as under 1 ms counts as 1 ms)."""
+    est = max(step_ms, 1.0)
     return (max(steps, math.ceil(PER_CONFIG_SECONDS * 1e3 / est)),
             max(warmup, math.ceil(PER_CONFIG_WARM_SECONDS * 1e3 / est)))
 

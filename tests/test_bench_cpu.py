@@ -90,6 +90,6 @@ def test_block_sizes():
     timed steps after 0.15 s of warm-up."""
     assert bench.block_sizes(8.0, 6, 2) == (38, 19)        # an 8 ms step: 0.3 s and 0.15 s decide
     assert bench.block_sizes(250.0, 6, 2) == (6, 2)        # a 250 ms step: the minimum counts decide
-    assert bench.block_sizes(0.0, 6, 2)[0] >= 6            # a zero reading does not divide by zero
+    assert bench.block_sizes(0.0, 6, 2) == (300, 150)      # a zero reading counts as 1 ms
     s, w = bench.block_sizes(23.0, 6, 2)
     assert s * 23.0 >= 300.0 and w * 23.0 >= 150.0 and (s - 1) * 23.0 < 300.0
